@@ -1,0 +1,278 @@
+/*
+ * nvfp4_moe.h -- C ABI of the GB300 (sm_103a) NVFP4 Mixture-of-Experts layer.
+ *
+ * The layer, as the pages state the problem: E experts with top-k routing per
+ * token, hidden size H and intermediate size I; FP4 e2m1 operands with one FP8
+ * e4m3 scale per 16 elements along K plus one FP32 scale per tensor; BF16
+ * output.  Per token: route to k experts, run each expert's gate_up GEMM,
+ * SiLU-mul, requantise to NVFP4, run its down GEMM, and FINALIZE the k expert
+ * rows back into the token's BF16 row with the router weights.
+ *   - "Tracing the Failure: Debugging CUTLASS FP4 Tile Configurations on
+ *     Blackwell SM120", "The Broader Context": 256 experts, 8 per token,
+ *     decode expert GEMMs of about 32x2048x6144.
+ *   - same page, "Input Knowledge Required": one GEMM per expert inside one
+ *     grouped launch, with a problem size per expert.
+ *   - "Cracking the SM120 Shared Memory Ceiling: A Deep Dive into CUTLASS Tile
+ *     Configuration Debugging", "The Shared Memory Calculation": FP4 packed at
+ *     4 bits, one FP8 scale per 16 elements along K for both operands.
+ *   - "The CUTLASS Tile That Wouldn't Fit: Debugging EP8 on Blackwell SM120",
+ *     "The Crash": e2m1 x e2m1 -> bf16 grouped GEMM.
+ *   - "The Epilogue That Broke the Kernel: Tracing a CUTLASS Tile
+ *     Configuration Failure on Blackwell GPUs", "The Insight: FINALIZE vs
+ *     NONE": epilogue NONE stores the GEMM result, FINALIZE does more.
+ *
+ * Conventions for every call below.
+ *   - Every pointer argument is a DEVICE pointer unless its comment says host.
+ *     The caller allocates and owns all memory; the library never allocates.
+ *     Where scratch is needed the caller passes a workspace of at least the
+ *     size the matching *_workspace_size() query returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream).  Calls return after enqueueing; results are ready when the
+ *     stream reaches them.
+ *   - Errors are returned, never thrown.  Argument checks happen on the host
+ *     before anything is launched; a call that returns an error has enqueued
+ *     nothing.  Device-side bounded waits that give up record MOE_ERR_TIMEOUT
+ *     in a device error word that moe_device_error() reads.
+ *   - Raw bf16 values are passed as uint16_t bit patterns.
+ *
+ * Data layouts.
+ *   NVFP4 codes: uint8 [rows][K/2], row-major, element 2i in the low nibble
+ *     and 2i+1 in the high nibble of byte i.
+ *   Linear scales: uint8 (e4m3) [rows][K/16], row-major.
+ *   Tiled scales (what the GEMM reads): rows in blocks of 128, scale columns
+ *     c = k/16 in groups of 4; each (row block, column group) is a 512-byte
+ *     atom, atoms ordered row-block-major; inside an atom the scale of (r, c)
+ *     sits at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4.  Requires
+ *     K % 64 == 0 and a row allocation that is a multiple of 128.
+ *   Routed rows ("padded rows"): the R = T*k (token, slot) pairs sorted stably
+ *     by expert; expert e owns rows [P_e, P_e + M_e) where M_e is its count
+ *     and P_e = sum over e' < e of ceil(M_e' / 128) * 128.  The rows between
+ *     P_e + M_e and P_{e+1} are padding: never read into any result.
+ *   Prepared expert weights: codes [E][N][K/2] and tiled scales over E*N rows
+ *     (N % 128 == 0).  For the gate_up weights (N = 2I) the rows are
+ *     interleaved in blocks of 64: prepared row 128*b + j is gate row 64*b + j
+ *     and prepared row 128*b + 64 + j is up row 64*b + j (j < 64).
+ */
+#ifndef NVFP4_MOE_H
+#define NVFP4_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, non-positive or inconsistent size, k > E, ... */
+  MOE_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned (TMA and vector access need it) */
+  MOE_ERR_UNSUPPORTED = 3, /* shape outside what the kernels implement (K % 64, N % 128, E > 1024, ...) */
+  MOE_ERR_RESOURCE = 4,    /* the tile configuration does not fit shared or tensor memory */
+  MOE_ERR_CUDA = 5,        /* a CUDA runtime or driver call failed (launch, attribute, tensor map) */
+  MOE_ERR_TIMEOUT = 6,     /* a device-side bounded wait gave up (see moe_device_error) */
+  MOE_ERR_WORKSPACE = 7    /* workspace pointer null or smaller than the size query asks for */
+} moe_status;
+
+enum { MOE_SF_LINEAR = 0, MOE_SF_TILED = 1 };
+enum { MOE_IN_BF16 = 0, MOE_IN_F32 = 1 };
+enum { MOE_EPI_NONE = 0, MOE_EPI_SILU_MUL_QUANT = 1, MOE_EPI_FINALIZE = 2 };
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(int status);
+
+/* ABI version of this header; bumped on any incompatible change. */
+MOE_API int moe_abi_version(void);
+
+/* Reads and clears the device error word written by bounded waits that gave
+ * up: *code receives a moe_status (MOE_OK if none), *where a kernel-specific
+ * location tag.  Synchronises the device.  Host pointers. */
+MOE_API moe_status moe_device_error(int32_t* code, int32_t* where);
+
+/* Bound, in nanoseconds, of every device-side wait of the grouped GEMM
+ * (default 2 s; 0 restores the default).  A wait that runs out records
+ * MOE_ERR_TIMEOUT and its kernel returns early. */
+MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook: bit 0 makes the next grouped-GEMM launches skip filling their
+ * first pipeline stage, so the bounded-wait path can be exercised without
+ * faulting anything.  0 (the default) for normal operation. */
+MOE_API void moe_debug_set_flags(int flags);
+
+/* Upper bound, for the caller's allocation, of the padded routed rows of R
+ * routed rows over E experts: R + 127 * min(E, R), rounded up to 128. */
+MOE_API int64_t moe_padded_rows_max(int64_t routed_rows, int E);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_permute -- top-k routing and the stable permutation by expert.
+ *   "Tracing the Failure ...", "The Broader Context" (top-k of E experts per
+ *   token) and "Input Knowledge Required" (rows grouped per expert).
+ * For each token t: the k experts of largest logit (ties to the lower expert
+ * index), in descending order, and router weights w = softmax of the k
+ * selected logits (max-subtracted, exponentials summed in slot order, all
+ * FP32, exp by Cody-Waite reduction and a degree-7 Taylor polynomial).  Then
+ * the expanded items i = t*k + j are sorted stably by expert.
+ *   logits            f32 [T][E]
+ *   topk_id           i32 [T][k]   out
+ *   topk_w            f32 [T][k]   out
+ *   expert_offsets    i32 [E+1]    out: start of expert e among the R sorted items
+ *   perm_to_expanded  i32 [R]      out: item i stored at sorted position p
+ *   expanded_to_perm  i32 [R]      out: inverse of perm_to_expanded
+ *   expanded_to_row   i32 [R]      out: padded routed row of item i
+ *                                       (P_e + expanded_to_perm[i] - expert_offsets[e])
+ *   ws / ws_bytes     workspace of moe_route_permute_workspace_size(T, E, k) bytes
+ * Requires 1 <= k <= min(E, 32), E <= 1024, T >= 1.  Deterministic.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_route_permute_workspace_size(int T, int E, int k);
+MOE_API moe_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* topk_id, float* topk_w,
+                             int32_t* expert_offsets, int32_t* perm_to_expanded, int32_t* expanded_to_perm,
+                             int32_t* expanded_to_row, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * nvfp4_quantize -- NVFP4 quantisation of rows of a bf16 or f32 matrix.
+ *   "Cracking the SM120 Shared Memory Ceiling ...", "The Shared Memory
+ *   Calculation" (4-bit values, one FP8 scale per 16 elements along K).
+ * Decode multiplier per group of rows: s = amax/(6*448) (1 when amax = 0),
+ * computed here when dynamic_scale != 0 and written to tensor_scale[g], else
+ * read from tensor_scale[g].  Per 16-element block: scale
+ * sf = e4m3_rn_satfinite(amax_16 / (6*s)); d = e4m3(sf)*s; codes
+ * q = e2m1_rn_satfinite(x * (1/d)) (ties to even, magnitude-0 results +0),
+ * all zero when d == 0.  The represented value is e2m1(q)*e4m3(sf)*s.
+ *   x             [src_rows][K], bf16 bits (in_dtype MOE_IN_BF16) or f32
+ *   groups        src_rows is split into `groups` equal consecutive groups, each
+ *                 with its own scale (1 for an activation tensor, E for weights)
+ *   tensor_scale  f32 [groups]: in (static) or out (dynamic)
+ *   n_items       number of output rows to write
+ *   src_div       item i reads source row i / src_div (1 = row i)
+ *   dst_row       i32 [n_items] or NULL: item i is written to output row
+ *                 dst_row[i] (NULL: row i)
+ *   codes         u8 [dst_rows_alloc][K/2]           out
+ *   sf            u8, linear [dst_rows_alloc][K/16] or tiled over
+ *                 dst_rows_alloc rows (sf_layout)   out
+ *   ws / ws_bytes workspace of nvfp4_quantize_workspace_size(groups) bytes
+ * Requires K % 16 == 0 (K % 64 == 0 and dst_rows_alloc % 128 == 0 for tiled),
+ * src_rows % groups == 0.  Rows of the output not named by any item are left
+ * untouched.  Deterministic, bit-exact with the definition above.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t nvfp4_quantize_workspace_size(int groups);
+MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows, int K, int groups, float* tensor_scale,
+                          int dynamic_scale, int64_t n_items, int src_div, const int32_t* dst_row,
+                          uint8_t* codes, uint8_t* sf, int sf_layout, int64_t dst_rows_alloc, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_grouped_gemm_nvfp4 -- the expert-grouped block-scaled FP4 GEMM.
+ *   "Tracing the Failure ...", "Input Knowledge Required" (one GEMM per expert
+ *   in one grouped launch); "The CUTLASS Tile That Wouldn't Fit ...", "The
+ *   Crash" (e2m1 x e2m1 -> bf16); "The Epilogue That Broke the Kernel ...",
+ *   "The Insight: FINALIZE vs NONE" (epilogues).
+ * For expert e and each of its routed rows r (padded-row layout, counts from
+ * expert_offsets):
+ *   Y[r][n] = a_scale[0] * b_scale[e] * sum_k dq(A[r][k]) * dq(B[e][n][k])
+ * with FP32 accumulation on the tensor cores.  Epilogues:
+ *   MOE_EPI_NONE: out = bf16 [a_rows_alloc][N], Y rounded to nearest even;
+ *     padding rows untouched.
+ *   MOE_EPI_SILU_MUL_QUANT (gate_up; B prepared with interleaved gate/up rows,
+ *     N = 2I): h[r][i] = silu(Y_gate) * Y_up in FP32, then NVFP4-quantised
+ *     with the static decode multiplier ep->h_scale into ep->h_codes
+ *     [a_rows_alloc][I/2] and tiled ep->h_sf; ep->h_scale_out (device f32,
+ *     optional) receives h_scale; ep->h_f32 (optional) receives the FP32 h.
+ *     `out` is unused.
+ *   MOE_EPI_FINALIZE (down): out = bf16 [ep->T][N],
+ *     out[t][n] = sum_j topk_w[t][j] * Y[row of item t*k+j][n], summed in FP32
+ *     (atomically: the order of the k terms is not fixed) and rounded once.
+ * Arguments:
+ *   a_codes/a_sf  activations, padded-row layout, tiled scales, a_rows_alloc rows
+ *   a_scale       f32 [1] decode multiplier of A
+ *   b_codes/b_sf  prepared expert weights [E][N][K/2], tiled scales
+ *   b_scale       f32 [E]
+ *   expert_offsets i32 [E+1] (as moe_route_permute writes them)
+ *   ep            host pointer to epilogue arguments (NULL for NONE)
+ *   ws / ws_bytes workspace of moe_grouped_gemm_workspace_size(...) bytes
+ * Requires K % 64 == 0, N % 128 == 0 (and N/2 % 64 == 0 for SILU_MUL_QUANT),
+ * E <= 1024, a_rows_alloc % 128 == 0, all pointers 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  /* MOE_EPI_SILU_MUL_QUANT */
+  float h_scale;
+  float* h_scale_out;
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+  float* h_f32;
+  /* MOE_EPI_FINALIZE */
+  const int32_t* perm_to_expanded;
+  const float* topk_w;
+  int32_t T;
+  int32_t k;
+} moe_epilogue_args;
+
+MOE_API size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int N);
+MOE_API moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                  const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,
+                                  const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,
+                                  int epilogue, const moe_epilogue_args* ep, void* out, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_finalize -- standalone FINALIZE: the router-weighted sum of each
+ * token's k expert rows back into one BF16 row.
+ *   "The Epilogue That Broke the Kernel ...", "The Insight: FINALIZE vs NONE";
+ *   "Cracking the SM120 Shared Memory Ceiling ...", "The Shared Memory
+ *   Calculation" (FP32 accumulator, BF16 output).
+ *   out[t][n] = bf16_rn( sum_{j<k} topk_w[t][j] * y[row_of_item[t*k+j]][n] ),
+ *   summed in FP32 in slot order (deterministic).
+ *   y            bf16 [*][N]
+ *   topk_w       f32 [T][k]
+ *   row_of_item  i32 [T*k]: the row of y holding item t*k+j (expanded_to_perm
+ *                for an unpadded y, expanded_to_row for a padded one)
+ *   out          bf16 [T][N]
+ * Requires N % 8 == 0.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_finalize(const uint16_t* y, const float* topk_w, const int32_t* row_of_item, int T, int k, int N,
+                        uint16_t* out, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_forward -- the fused MoE layer: route + permute, quantise x into the
+ * routed rows, gate_up GEMM with SiLU-mul + requantise epilogue, down GEMM
+ * with FINALIZE epilogue.  Same definitions as the calls above.
+ *   x        bf16 [T][H]
+ *   logits   f32 [T][E]
+ *   w        host pointer to the prepared expert weights
+ *   h_scale  static decode multiplier of the requantised intermediate (host value)
+ *   out      bf16 [T][H]
+ *   ws       workspace of moe_forward_workspace_size(T, E, k, H, I) bytes; its
+ *            layout (moe_forward_workspace_layout) exposes the intermediates.
+ * Requires H % 128 == 0, I % 64 == 0, plus the requirements above.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const uint8_t* w13_codes; /* [E][2I][H/2], gate/up interleaved */
+  const uint8_t* w13_sf;    /* tiled over E*2I rows */
+  const float* w13_scale;   /* [E] */
+  const uint8_t* w2_codes;  /* [E][H][I/2] */
+  const uint8_t* w2_sf;     /* tiled over E*H rows */
+  const float* w2_scale;    /* [E] */
+} moe_weights;
+
+/* Byte offsets of each intermediate inside the moe_forward workspace. */
+typedef struct {
+  size_t topk_id, topk_w, expert_offsets, perm_to_expanded, expanded_to_perm, expanded_to_row;
+  size_t x_scale, x_codes, x_sf, h_scale, h_codes, h_sf, route_ws, quant_ws, gemm_ws;
+  int64_t padded_rows; /* rows allocated for the routed-row buffers */
+  size_t total;
+} moe_forward_layout;
+
+MOE_API size_t moe_forward_workspace_size(int T, int E, int k, int H, int I);
+MOE_API moe_status moe_forward_workspace_layout(int T, int E, int k, int H, int I, moe_forward_layout* layout);
+MOE_API moe_status moe_forward(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k, int H,
+                       int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_MOE_H */

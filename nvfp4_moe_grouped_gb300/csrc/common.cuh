@@ -1,0 +1,274 @@
+// common.cuh -- shared device helpers of the GB300 NVFP4 MoE kernels (sm_103a).
+//
+// Inline-PTX wrappers for mbarriers, TMA, tcgen05 (tensor memory, block-scaled
+// MMA) and the small scalar pieces the kernels share: the NVFP4 encoders, the
+// routing exp, bf16 rounding.  Nothing here allocates memory.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4_moe.h"
+
+#define MOE_DEVINL __device__ __forceinline__
+
+namespace moe {
+
+// ----------------------------------------------------------------------------
+// Host-side plumbing shared by the translation units (defined in capi.cu).
+// ----------------------------------------------------------------------------
+int32_t* device_error_word();          // device address of {code, where}
+uint64_t wait_timeout_ns();            // bound of every device-side wait
+int num_sms();                          // SM count of the current device
+moe_status check_launch();              // maps cudaGetLastError to a status
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------------------------
+// Scalars
+// ----------------------------------------------------------------------------
+MOE_DEVINL uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Records the first error of a launch; later ones are dropped.
+MOE_DEVINL void record_error(int32_t* err, int32_t code, int32_t where) {
+  if (atomicCAS(err, 0, code) == 0) atomicExch(err + 1, where);
+}
+
+// exp for the router weights: Cody-Waite reduction x = n ln2 + r with ln 2
+// split into an FP32 head and tail, then the degree-7 Taylor polynomial of
+// e^r in Horner form with fused multiply-adds, then an exact scaling by 2^n.
+// Results below e^-86 flush to 0 (all inputs here are <= 0).  Every operation
+// is correctly rounded, so the host restatement gives identical bits.
+MOE_DEVINL float route_exp(float x) {
+  const float kLog2e = 0x1.715476p+0f;
+  const float kLn2Hi = 0x1.62e43p-1f;
+  const float kLn2Lo = -0x1.05c61p-29f;
+  if (!(x >= -86.0f)) return 0.0f;
+  if (x > 88.0f) return __int_as_float(0x7f800000);
+  float n = rintf(__fmul_rn(x, kLog2e));
+  float r = __fmaf_rn(-n, kLn2Hi, x);
+  r = __fmaf_rn(-n, kLn2Lo, r);
+  float p = 0x1.a01a02p-13f;                 // 1/7!
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);      // 1/6!
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);       // 1/5!
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);       // 1/4!
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);       // 1/3!
+  p = __fmaf_rn(p, r, 0x1p-1f);              // 1/2!
+  p = __fmaf_rn(p, r, 1.0f);                 // 1/1!
+  p = __fmaf_rn(p, r, 1.0f);                 // 1/0!
+  float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+  return __fmul_rn(p, two_n);
+}
+
+// e2m1 code of v: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even
+// code, saturating above 6; a magnitude-0 result is +0.
+MOE_DEVINL uint32_t e2m1_encode(float v) {
+  float a = fabsf(v);
+  uint32_t c;
+  if (a <= 0.25f) c = 0;
+  else if (a < 0.75f) c = 1;
+  else if (a <= 1.25f) c = 2;
+  else if (a < 1.75f) c = 3;
+  else if (a <= 2.5f) c = 4;
+  else if (a < 3.5f) c = 5;
+  else if (a <= 5.0f) c = 6;
+  else c = 7;
+  if (c != 0 && v < 0.0f) c |= 8u;
+  return c;
+}
+
+// e4m3 (fn) scale byte of a non-negative value: round to nearest even,
+// saturating to 448.
+MOE_DEVINL uint32_t e4m3_encode_satfinite(float v) {
+  __nv_fp8_storage_t s = __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(s) & 0xFFu;
+}
+
+MOE_DEVINL float e4m3_decode(uint32_t byte) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// The NVFP4 scale of one 16-element block with decode multiplier s.
+// Returns the e4m3 byte and the reciprocal multiplier (0 when the block's
+// decoded scale is 0, which zeroes every code of the block).
+MOE_DEVINL uint32_t nvfp4_block_scale(float amax, float s, float* recip) {
+  float sf_f = __fdiv_rn(amax, __fmul_rn(6.0f, s));
+  uint32_t sf = e4m3_encode_satfinite(sf_f);
+  float d = __fmul_rn(e4m3_decode(sf), s);
+  *recip = (d == 0.0f) ? 0.0f : __frcp_rn(d);
+  return sf;
+}
+
+MOE_DEVINL uint32_t nvfp4_code(float x, float recip) {
+  return (recip == 0.0f) ? 0u : e2m1_encode(__fmul_rn(x, recip));
+}
+
+MOE_DEVINL float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+MOE_DEVINL uint16_t float_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// Byte offset of scale (row r, column c) in the tiled scale layout.
+MOE_DEVINL int64_t tiled_sf_offset(int64_t r, int c, int K) {
+  int64_t atom = (r >> 7) * (K >> 6) + (c >> 2);
+  return atom * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// ----------------------------------------------------------------------------
+// Shared memory, mbarriers
+// ----------------------------------------------------------------------------
+MOE_DEVINL uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+MOE_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+MOE_DEVINL void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+MOE_DEVINL void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+MOE_DEVINL void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+MOE_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Gives up
+// (returns false) after timeout_ns, or early once *abort is set by another
+// role of the same CTA.
+MOE_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// TMA and bulk copies (global -> shared, completion on an mbarrier)
+// ----------------------------------------------------------------------------
+MOE_DEVINL uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+MOE_DEVINL uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+MOE_DEVINL void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+MOE_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ----------------------------------------------------------------------------
+// tcgen05: tensor memory and the block-scaled MMA
+// ----------------------------------------------------------------------------
+MOE_DEVINL void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+MOE_DEVINL void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
+MOE_DEVINL void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+MOE_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MOE_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] x B[smem]^T with e2m1 operands and ue4m3 scales per 16
+// K-elements read from tensor memory (M = 128, N from the descriptor, K = 64).
+MOE_DEVINL void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
+                             uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
+MOE_DEVINL void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Copies a 32-row x 16-byte shared-memory matrix into 4 TMEM columns of lanes
+// 0-31, replicated into the lanes of all four warp quadrants.
+MOE_DEVINL void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Each thread of the warp loads 32 consecutive 32-bit columns of its lane.
+MOE_DEVINL void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+MOE_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format, version 1).
+//   start: byte address; lbo/sbo: leading/stride byte offsets; layout:
+//   0 = no swizzle, 2 = 128-byte swizzle.
+MOE_DEVINL uint64_t smem_desc(uint32_t start, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((start >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::mxf4nvf4: e2m1 A and B (format 1), both
+// K-major, ue4m3 scales (bit 23 = 0), dense, M = 128.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+}  // namespace moe

@@ -1,0 +1,563 @@
+// grouped_gemm.cu -- the expert-grouped NVFP4 GEMM on the 5th-generation
+// tensor cores (tcgen05, kind::mxf4nvf4, e2m1 x e2m1 with ue4m3 scales per 16
+// K-elements, FP32 accumulation in tensor memory).
+//
+// What it computes: "Tracing the Failure: Debugging CUTLASS FP4 Tile
+// Configurations on Blackwell SM120", section "Input Knowledge Required" (one
+// GEMM per expert inside a single grouped launch, one problem size per
+// expert); "The CUTLASS Tile That Wouldn't Fit: Debugging EP8 on Blackwell
+// SM120", section "The Crash" (e2m1 x e2m1 -> bf16); epilogues NONE and
+// FINALIZE from "The Epilogue That Broke the Kernel: Tracing a CUTLASS Tile
+// Configuration Failure on Blackwell GPUs", section "The Insight: FINALIZE vs
+// NONE", plus the gate_up epilogue (SiLU-mul and NVFP4 requantisation).
+//
+// Design (GB300, one CTA per SM, persistent):
+//   * Operand roles are swapped relative to the row-major problem: the 128
+//     weight rows of a tile are the MMA M dimension and the expert's routed
+//     token rows (up to 128) are MMA N.  At decode an expert sees 4-64 rows,
+//     so every weight tile is streamed from HBM exactly once per 128 routed
+//     rows and the tensor core never waits on padding.
+//   * Work unit = (expert, 128-row block of its routed rows, 128-row weight
+//     tile), full K.  Units are ordered expert-major so the ~150 CTAs running
+//     together share each expert's token tile in L2.  CTA c takes units c,
+//     c + grid, ...
+//   * Warp roles: warp 0 issues TMA (weights and tokens: 2D tensor maps with
+//     128-byte swizzle; scales: 1D bulk copies of the tiled 512-byte atoms),
+//     warp 1 owns tensor memory and issues tcgen05.cp (scales -> TMEM) and
+//     tcgen05.mma, warps 2-5 drain the accumulator (tcgen05.ld) and run the
+//     epilogue.  A 5-stage shared-memory ring (36 KB per stage) keeps ~180 KB
+//     of loads in flight per SM; two TMEM accumulators let the epilogue of
+//     one unit overlap the mainloop of the next.
+//   * Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT in the
+//     device error word, lets its own copies and MMAs finish, frees its tensor
+//     memory and returns.
+#include "common.cuh"
+
+namespace moe {
+moe_status launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t st);
+
+namespace {
+
+constexpr int kBM = 128;                       // weight rows per tile (MMA M)
+constexpr int kBK = 256;                       // K elements per stage (128 bytes per row)
+constexpr int kBNMax = 128;                    // routed rows per tile (MMA N <= 128)
+constexpr int kStages = 5;
+constexpr int kWStageBytes = kBM * kBK / 2;    // 16 KB
+constexpr int kXStageBytes = kBNMax * kBK / 2; // 16 KB
+constexpr int kSfStageBytes = 4 * 512;         // 4 scale atoms (one per 64-element K step)
+constexpr int kThreads = 192;
+constexpr int kMaxExperts = 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kBNMax;          // per accumulator buffer
+constexpr uint32_t kSfTmemBase = 2 * kAccCols; // scale slots after the two accumulators
+constexpr uint32_t kSfSlotCols = 32;           // 16 columns weight scales + 16 columns token scales
+static_assert(kSfTmemBase + kStages * kSfSlotCols <= kTmemCols, "tensor memory budget");
+
+struct SmemLayout {
+  static constexpr int w = 0;
+  static constexpr int x = w + kStages * kWStageBytes;
+  static constexpr int sfw = x + kStages * kXStageBytes;
+  static constexpr int sfx = sfw + kStages * kSfStageBytes;
+  static constexpr int epi = sfx + kStages * kSfStageBytes;            // float [32][65]
+  static constexpr int tok_t = epi + 32 * 65 * 4;                       // int [128]
+  static constexpr int tok_w = tok_t + kBNMax * 4;                      // float [128]
+  static constexpr int bars = tok_w + kBNMax * 4;                       // uint64 [2*kStages + 5]
+  static constexpr int misc = bars + (2 * kStages + 5) * 8;             // tmem base, abort
+  static constexpr int sched = misc + 16;                               // int [3][kMaxExperts+1]
+  static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
+};
+constexpr int kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct GemmParams {
+  const uint8_t* w_sf;        // tiled scales of the weights (E*N rows)
+  const uint8_t* x_sf;        // tiled scales of the routed rows
+  const float* x_scale;       // [1]
+  const float* w_scale;       // [E]
+  const int32_t* expert_offsets;
+  int E, N, K;
+  int epilogue;
+  void* out;                  // NONE: bf16 [rows][N]; FINALIZE: f32 accumulator [T][N]
+  float h_scale;
+  float* h_scale_out;
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+  float* h_f32;
+  const int32_t* perm_to_expanded;
+  const float* topk_w;
+  int k;
+  int T;
+  int64_t rows_alloc;         // rows of the routed-row operand (bounds every access to it)
+  int32_t* err;
+  uint64_t timeout_ns;
+  int debug_flags;            // bit 0: the producer skips the first stage (bounded-wait test hook)
+};
+
+struct Unit {
+  int e, nb, mt, rows, n_mma, x_row, w_row, m_off;
+  bool valid;  // false when the offsets place the unit outside the routed-row allocation
+};
+
+MOE_DEVINL int find_expert(const int* start, int E, int u) {
+  int lo = 0, hi = E;  // start[lo] <= u < start[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (start[mid] <= u) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MT,
+                            int64_t rows_alloc) {
+  Unit d;
+  d.e = find_expert(unit_start, E, u);
+  int local = u - unit_start[d.e];
+  d.nb = local / MT;
+  d.mt = local - d.nb * MT;
+  int m_e = off[d.e + 1] - off[d.e];
+  d.rows = min(kBNMax, m_e - d.nb * kBNMax);
+  d.n_mma = d.rows <= 32 ? 32 : (d.rows <= 64 ? 64 : 128);
+  d.x_row = pad_start[d.e] + d.nb * kBNMax;
+  d.m_off = off[d.e] + d.nb * kBNMax;
+  d.w_row = 0;  // set by caller (needs N)
+  d.valid = d.rows > 0 && static_cast<int64_t>(d.x_row) + kBNMax <= rows_alloc;
+  return d;
+}
+
+// Named barrier 1 over the 128 epilogue threads.
+MOE_DEVINL void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// True on every epilogue thread if `pred` holds on any of them (barrier 1 with an OR reduction).
+MOE_DEVINL bool epi_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                        const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_w = smem + SmemLayout::w;
+  uint8_t* s_x = smem + SmemLayout::x;
+  uint8_t* s_sfw = smem + SmemLayout::sfw;
+  uint8_t* s_sfx = smem + SmemLayout::sfx;
+  float* s_epi = reinterpret_cast<float*>(smem + SmemLayout::epi);
+  int* s_tok_t = reinterpret_cast<int*>(smem + SmemLayout::tok_t);
+  float* s_tok_w = reinterpret_cast<float*>(smem + SmemLayout::tok_w);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SmemLayout::misc + 4);
+  int* unit_start = reinterpret_cast<int*>(smem + SmemLayout::sched);
+  int* pad_start = unit_start + (kMaxExperts + 1);
+  int* off = pad_start + (kMaxExperts + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, N = p.N, K = p.K;
+  const int MT = N / kBM;
+  const int KT = (K + kBK - 1) / kBK;
+
+  // ---- prologue: barriers, tensor memory, work list --------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0) {
+    // unit_start[e]: first unit of expert e; pad_start[e]: first padded row.
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int units = 0, pads = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      int m = __ldg(p.expert_offsets + e + 1) - __ldg(p.expert_offsets + e);
+      int blocks = (m + kBNMax - 1) / kBNMax;
+      units += blocks * MT;
+      pads += blocks * kBNMax;
+    }
+    int iu = units, ip = pads;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int yu = __shfl_up_sync(0xffffffffu, iu, o), yp = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) { iu += yu; ip += yp; }
+    }
+    int ru = iu - units, rp = ip - pads;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      int o0 = __ldg(p.expert_offsets + e), o1 = __ldg(p.expert_offsets + e + 1);
+      unit_start[e] = ru;
+      pad_start[e] = rp;
+      off[e] = o0;
+      int blocks = (o1 - o0 + kBNMax - 1) / kBNMax;
+      ru += blocks * MT;
+      rp += blocks * kBNMax;
+    }
+    if (lane == 31) {
+      unit_start[E] = iu;
+      pad_start[E] = ip;
+      off[E] = __ldg(p.expert_offsets + E);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int total_units = unit_start[E];
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      bool skip_once = (p.debug_flags & 1) != 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        Unit d = decode_unit(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+        if (!d.valid) continue;
+        const int w_row = d.e * N + d.mt * kBM;
+        const uint8_t* sfw_src = p.w_sf + static_cast<int64_t>(w_row / 128) * (K / 64) * 512;
+        const uint8_t* sfx_src = p.x_sf + static_cast<int64_t>(d.x_row / 128) * (K / 64) * 512;
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 1);
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          const int steps = min(4, (K - kt * kBK) / 64);
+          if (skip_once) {
+            skip_once = false;  // test hook: this stage is never filled
+          } else {
+            const uint32_t bytes = kWStageBytes + d.n_mma * (kBK / 2) + 2 * steps * 512;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            tma_load_2d(s_w + stage * kWStageBytes, &tm_w, &full[stage], kt * (kBK / 2), w_row, pol_w);
+            for (int q = 0; q < d.n_mma / 32; ++q)
+              tma_load_2d(s_x + stage * kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage], kt * (kBK / 2),
+                          d.x_row + 32 * q, pol_x);
+            bulk_load(s_sfw + stage * kSfStageBytes, sfw_src + kt * 4 * 512, steps * 512, &full[stage], pol_w);
+            bulk_load(s_sfx + stage * kSfStageBytes, sfx_src + kt * 4 * 512, steps * 512, &full[stage], pol_x);
+            issued[stage] += 1;
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Let every copy this CTA started land before the CTA can exit.
+      int zero = 0;
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] > 0)
+          mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.timeout_ns,
+                            reinterpret_cast<volatile int*>(&zero));
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc_i = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++acc_i) {
+        Unit d = decode_unit(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+        if (!d.valid) { --acc_i; continue; }
+        const int b = acc_i & 1;
+        if (!mbar_wait_bounded(&acc_empty[b], ((acc_i >> 1) & 1) ^ 1u, p.timeout_ns, s_abort)) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 2);
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * kAccCols;
+        const uint32_t idesc = idesc_mxf4nvf4(d.n_mma);
+        for (int kt = 0; kt < KT; ++kt) {
+          if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 3);
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int steps = min(4, (K - kt * kBK) / 64);
+          const uint32_t sf_col = tmem_base + kSfTmemBase + stage * kSfSlotCols;
+          const uint32_t sfw_addr = smem_u32(s_sfw + stage * kSfStageBytes);
+          const uint32_t sfx_addr = smem_u32(s_sfx + stage * kSfStageBytes);
+          for (int g = 0; g < steps; ++g) {
+            tmem_cp_32x128b_x4(sf_col + 4 * g, smem_desc(sfw_addr + 512 * g, 0, 128, 0));
+            tmem_cp_32x128b_x4(sf_col + 16 + 4 * g, smem_desc(sfx_addr + 512 * g, 0, 128, 0));
+          }
+          const uint32_t w_addr = smem_u32(s_w + stage * kWStageBytes);
+          const uint32_t x_addr = smem_u32(s_x + stage * kXStageBytes);
+          for (int g = 0; g < steps; ++g) {
+            const uint64_t adesc = smem_desc(w_addr + 32 * g, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(x_addr + 32 * g, 16, 1024, 2);
+            mma_mxf4nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * g, sf_col + 16 + 4 * g, (kt | g) != 0);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[b]);
+      }
+      // Every MMA and scale copy this thread issued has completed once this arrives.
+      mma_commit(mma_done);
+      int zero = 0;
+      mbar_wait_bounded(mma_done, 0, p.timeout_ns, reinterpret_cast<volatile int*>(&zero));
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    const int m = 32 * q + lane;       // weight row of the tile owned by this thread
+    const int et = threadIdx.x - 64;   // 0..127
+    const float x_scale = __ldg(p.x_scale);
+    if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && et == 0) *p.h_scale_out = p.h_scale;
+    int acc_i = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
+      Unit d = decode_unit(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+      if (!d.valid) {
+        if (et == 0) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+        --acc_i;
+        continue;
+      }
+      const int b = acc_i & 1;
+      const bool got = mbar_wait_bounded(&acc_full[b], (acc_i >> 1) & 1, p.timeout_ns, s_abort);
+      // The four epilogue warps decide together, so none is left waiting on a
+      // named barrier that the others have abandoned.
+      if (epi_any(!got)) {
+        if (et == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 4);
+          *s_abort = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const float alpha = x_scale * __ldg(p.w_scale + d.e);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kAccCols;
+      if (p.epilogue == MOE_EPI_FINALIZE) {
+        if (et < d.rows) {
+          const int ex = __ldg(p.perm_to_expanded + d.m_off + et);
+          const bool in_range = ex >= 0 && ex < p.T * p.k;
+          if (!in_range) record_error(p.err, MOE_ERR_INVALID_ARG, 6);
+          s_tok_t[et] = in_range ? ex / p.k : -1;
+          s_tok_w[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
+        }
+        epi_bar();
+      }
+      for (int j0 = 0; j0 < d.rows; j0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + j0, r);
+        tmem_ld_wait();
+        const int jn = min(32, d.rows - j0);
+        if (p.epilogue == MOE_EPI_NONE) {
+          uint16_t* out = static_cast<uint16_t*>(p.out);
+          const int64_t col = static_cast<int64_t>(d.mt) * kBM + m;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            if (jj < jn)
+              out[static_cast<int64_t>(d.x_row + j0 + jj) * N + col] =
+                  float_to_bf16_bits(alpha * __uint_as_float(r[jj]));
+        } else if (p.epilogue == MOE_EPI_FINALIZE) {
+          float* acc = static_cast<float*>(p.out);
+          const int64_t col = static_cast<int64_t>(d.mt) * kBM + m;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            if (jj < jn && s_tok_t[j0 + jj] >= 0)
+              atomicAdd(acc + static_cast<int64_t>(s_tok_t[j0 + jj]) * N + col,
+                        s_tok_w[j0 + jj] * __uint_as_float(r[jj]));
+        } else {
+          // gate_up tile: rows 0-63 are gate rows, rows 64-127 the matching up rows.
+          const int I = N / 2;
+          if (q >= 2) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) s_epi[jj * 65 + (m - 64)] = alpha * __uint_as_float(r[jj]);
+          }
+          epi_bar();
+          if (q < 2) {
+            const int i = d.mt * 64 + m;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              if (jj >= jn) break;  // jn is the same on every lane
+              const float g = alpha * __uint_as_float(r[jj]);
+              const float up = s_epi[jj * 65 + m];
+              const float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), up);
+              const int64_t row = d.x_row + j0 + jj;
+              if (p.h_f32) p.h_f32[row * I + i] = h;
+              float amax = fabsf(h);
+#pragma unroll
+              for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+              float recip;
+              const uint32_t sfb = nvfp4_block_scale(amax, p.h_scale, &recip);
+              const uint32_t code = nvfp4_code(h, recip);
+              const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+              if ((lane & 1) == 0) p.h_codes[row * (I / 2) + i / 2] = static_cast<uint8_t>(code | (hi << 4));
+              if ((lane & 15) == 0) p.h_sf[tiled_sf_offset(row, i / 16, I)] = static_cast<uint8_t>(sfb);
+            }
+          }
+          epi_bar();
+        }
+      }
+      if (p.epilogue == MOE_EPI_FINALIZE) epi_bar();  // the token table is rewritten by the next unit
+      tc_fence_before();
+      mbar_arrive(&acc_empty[b]);
+    }
+  }
+  // (control reaches here on every path)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+// 2D map over a [rows][row_bytes] byte matrix, boxes of 128 bytes x box_rows,
+// 128-byte swizzle (the layout the tcgen05 K-major descriptors expect).
+bool make_code_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int& gemm_debug_flags() {
+  static int flags = 0;
+  return flags;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int N) {
+  if (epilogue != MOE_EPI_FINALIZE) return 0;
+  if (T < 1 || N < 1) return 0;
+  size_t b = static_cast<size_t>(T) * N * sizeof(float);
+  return ((b + 255) / 256) * 256;
+}
+
+extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                             const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,
+                                             const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,
+                                             int epilogue, const moe_epilogue_args* ep, void* out, void* ws,
+                                             size_t ws_bytes, void* stream) {
+  if (!a_codes || !a_sf || !a_scale || !b_codes || !b_sf || !b_scale || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || a_rows_alloc < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_SILU_MUL_QUANT && epilogue != MOE_EPI_FINALIZE)
+    return MOE_ERR_INVALID_ARG;
+  if (E > kMaxExperts || K % 64 || N % kBM || a_rows_alloc % 128) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(E) * N > 0x7FFFFFFF || a_rows_alloc > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(b_codes) || !aligned16(b_sf)) return MOE_ERR_MISALIGNED;
+  GemmParams p{};
+  p.w_sf = b_sf;
+  p.x_sf = a_sf;
+  p.x_scale = a_scale;
+  p.w_scale = b_scale;
+  p.expert_offsets = expert_offsets;
+  p.E = E;
+  p.N = N;
+  p.K = K;
+  p.epilogue = epilogue;
+  if (epilogue == MOE_EPI_NONE) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out)) return MOE_ERR_MISALIGNED;
+    p.out = out;
+  } else if (epilogue == MOE_EPI_SILU_MUL_QUANT) {
+    if (!ep || !ep->h_codes || !ep->h_sf) return MOE_ERR_INVALID_ARG;
+    if ((N / 2) % 64) return MOE_ERR_UNSUPPORTED;
+    if (!(ep->h_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ep->h_codes) || !aligned16(ep->h_sf)) return MOE_ERR_MISALIGNED;
+    p.h_scale = ep->h_scale;
+    p.h_scale_out = ep->h_scale_out;
+    p.h_codes = ep->h_codes;
+    p.h_sf = ep->h_sf;
+    p.h_f32 = ep->h_f32;
+  } else {
+    if (!ep || !ep->perm_to_expanded || !ep->topk_w || !out || ep->T < 1 || ep->k < 1) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(out)) return MOE_ERR_MISALIGNED;
+    if (!ws || ws_bytes < moe_grouped_gemm_workspace_size(epilogue, ep->T, N)) return MOE_ERR_WORKSPACE;
+    if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+    p.out = ws;
+    p.perm_to_expanded = ep->perm_to_expanded;
+    p.topk_w = ep->topk_w;
+    p.k = ep->k;
+    p.T = ep->T;
+  }
+  p.rows_alloc = a_rows_alloc;
+  p.err = device_error_word();
+  p.timeout_ns = wait_timeout_ns();
+  p.debug_flags = gemm_debug_flags();
+  if (!p.err) return MOE_ERR_CUDA;
+
+  CUtensorMap tm_w, tm_x;
+  if (!make_code_map(&tm_w, b_codes, static_cast<uint64_t>(E) * N, K / 2, kBM)) return MOE_ERR_CUDA;
+  if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
+  if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return MOE_ERR_RESOURCE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t max_units = (a_rows_alloc / kBNMax) * (N / kBM);
+  int grid = num_sms();
+  if (grid < 1) return MOE_ERR_CUDA;
+  if (max_units < grid) grid = static_cast<int>(max_units);
+  if (epilogue == MOE_EPI_FINALIZE) {
+    if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tm_w, tm_x, p);
+  moe_status s = check_launch();
+  if (s != MOE_OK) return s;
+  if (epilogue == MOE_EPI_FINALIZE)
+    return launch_f32_to_bf16(static_cast<const float*>(ws), static_cast<uint16_t*>(out),
+                              static_cast<int64_t>(ep->T) * N, st);
+  return MOE_OK;
+}

@@ -1,0 +1,162 @@
+// quantize.cu -- NVFP4 quantisation (e2m1 codes, e4m3 scale per 16 elements,
+// FP32 decode multiplier per tensor or per group of rows).
+//
+// Format: "Cracking the SM120 Shared Memory Ceiling: A Deep Dive into CUTLASS
+// Tile Configuration Debugging", section "The Shared Memory Calculation" (FP4
+// packed at 4 bits per element, one FP8 scale per 16 elements along K).
+// Scale rule: s = amax/(6*448) per tensor; sf = e4m3(amax_16/(6 s));
+// q = e2m1(x / (e4m3(sf) s)) -- the reading stated in nvfp4_moe.h.
+//
+// HBM-bound: one read of x, one write of codes (K/2 bytes per row) and scales
+// (K/16 bytes per row).  One warp per output row; each lane owns 16-element
+// blocks lane, lane+32, ... so a warp streams contiguous 1 KB (bf16) chunks.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQuantWarps = 8;
+
+template <int IN_F32>
+MOE_DEVINL void load_block16(const void* x, int64_t row, int K, int blk, float (&v)[16]) {
+  if (IN_F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + row * K + blk * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float4 f = __ldg(p + i);
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + row * K + blk * 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      uint4 u = __ldg(p + i);
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+        v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+// Per-group absolute maximum: atomicMax on the bit pattern, which orders
+// non-negative floats like their values.
+template <int IN_F32>
+__global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, int64_t rows_per_group, int K,
+                                                   uint32_t* __restrict__ amax_bits) {
+  const int g = blockIdx.y;
+  const int64_t nblk = rows_per_group * (K / 16);
+  const int64_t base_row = static_cast<int64_t>(g) * rows_per_group;
+  float m = 0.0f;
+  for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < nblk;
+       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t r = base_row + b / (K / 16);
+    int c = static_cast<int>(b % (K / 16));
+    float v[16];
+    load_block16<IN_F32>(x, r, K, c, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(amax_bits + g, __float_as_uint(m));
+}
+
+__global__ void scale_from_amax_kernel(const uint32_t* __restrict__ amax_bits, int groups, float* __restrict__ scale) {
+  int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= groups) return;
+  float a = __uint_as_float(amax_bits[g]);
+  scale[g] = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+}
+
+template <int IN_F32, int TILED>
+__global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
+    const void* __restrict__ x, int64_t rows_per_group, int K, const float* __restrict__ scale, int64_t n_items,
+    int src_div, const int32_t* __restrict__ dst_row, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+  const int lane = threadIdx.x & 31;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (item >= n_items) return;
+  const int64_t src = item / src_div;
+  const int64_t dst = dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item;
+  const float s = __ldg(scale + src / rows_per_group);
+  const int nblk = K / 16;
+  for (int c = lane; c < nblk; c += 32) {
+    float v[16];
+    load_block16<IN_F32>(x, src, K, c, v);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float recip;
+    uint32_t sfb = nvfp4_block_scale(amax, s, &recip);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo |= nvfp4_code(v[i], recip) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hi |= nvfp4_code(v[8 + i], recip) << (4 * i);
+    *reinterpret_cast<uint2*>(codes + dst * (K / 2) + 8 * c) = make_uint2(lo, hi);
+    if (TILED)
+      sf[tiled_sf_offset(dst, c, K)] = static_cast<uint8_t>(sfb);
+    else
+      sf[dst * nblk + c] = static_cast<uint8_t>(sfb);
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t nvfp4_quantize_workspace_size(int groups) {
+  if (groups < 1) return 0;
+  return static_cast<size_t>((groups * 4 + 255) / 256) * 256;
+}
+
+extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows, int K, int groups,
+                                     float* tensor_scale, int dynamic_scale, int64_t n_items, int src_div,
+                                     const int32_t* dst_row, uint8_t* codes, uint8_t* sf, int sf_layout,
+                                     int64_t dst_rows_alloc, void* ws, size_t ws_bytes, void* stream) {
+  if (!x || !tensor_scale || !codes || !sf) return MOE_ERR_INVALID_ARG;
+  if (src_rows < 1 || K < 16 || groups < 1 || n_items < 0 || src_div < 1 || dst_rows_alloc < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (in_dtype != MOE_IN_BF16 && in_dtype != MOE_IN_F32) return MOE_ERR_INVALID_ARG;
+  if (sf_layout != MOE_SF_LINEAR && sf_layout != MOE_SF_TILED) return MOE_ERR_INVALID_ARG;
+  if (K % 16) return MOE_ERR_UNSUPPORTED;
+  if (sf_layout == MOE_SF_TILED && (K % 64 || dst_rows_alloc % 128)) return MOE_ERR_UNSUPPORTED;
+  if (src_rows % groups) return MOE_ERR_INVALID_ARG;
+  if ((n_items - 1) / src_div >= src_rows && n_items > 0) return MOE_ERR_INVALID_ARG;
+  if (!dst_row && n_items > dst_rows_alloc) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf)) return MOE_ERR_MISALIGNED;
+  if (dynamic_scale && (!ws || ws_bytes < nvfp4_quantize_workspace_size(groups))) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t rows_per_group = src_rows / groups;
+  if (dynamic_scale) {
+    uint32_t* amax = static_cast<uint32_t*>(ws);
+    if (cudaMemsetAsync(amax, 0, sizeof(uint32_t) * groups, st) != cudaSuccess) return MOE_ERR_CUDA;
+    int64_t nblk = rows_per_group * (K / 16);
+    int bx = static_cast<int>((nblk + 255) / 256);
+    int cap = (num_sms() * 8 + groups - 1) / groups;
+    if (bx > cap) bx = cap < 1 ? 1 : cap;
+    dim3 grid(bx, groups);
+    if (in_dtype == MOE_IN_F32)
+      amax_kernel<1><<<grid, 256, 0, st>>>(x, rows_per_group, K, amax);
+    else
+      amax_kernel<0><<<grid, 256, 0, st>>>(x, rows_per_group, K, amax);
+    scale_from_amax_kernel<<<(groups + 255) / 256, 256, 0, st>>>(amax, groups, tensor_scale);
+  }
+  if (n_items > 0) {
+    int64_t blocks = (n_items + kQuantWarps - 1) / kQuantWarps;
+    if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+    const bool f32 = in_dtype == MOE_IN_F32, tiled = sf_layout == MOE_SF_TILED;
+#define MOE_QLAUNCH(F, T)                                                                                     \
+  quantize_kernel<F, T><<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, st>>>(                          \
+      x, rows_per_group, K, tensor_scale, n_items, src_div, dst_row, codes, sf)
+    if (f32 && tiled) MOE_QLAUNCH(1, 1);
+    else if (f32) MOE_QLAUNCH(1, 0);
+    else if (tiled) MOE_QLAUNCH(0, 1);
+    else MOE_QLAUNCH(0, 0);
+#undef MOE_QLAUNCH
+  }
+  return check_launch();
+}

@@ -1,0 +1,237 @@
+// route_permute.cu -- top-k routing of tokens to experts and the stable
+// counting-sort permutation that groups the routed rows by expert.
+//
+// "Tracing the Failure: Debugging CUTLASS FP4 Tile Configurations on Blackwell
+// SM120", section "The Broader Context": 256 experts, 8 active per token;
+// section "Input Knowledge Required": one GEMM per expert over that expert's
+// rows.  Selection rule (largest logits, ties to the lower index) and weights
+// (softmax over the k selected logits) as stated in nvfp4_moe.h.
+//
+// Three launches, all deterministic:
+//   1. route_kernel: one warp per token does a warp-shuffle top-k over the E
+//      logits held in registers, the softmax of the selected k, and each block
+//      counts the expert histogram of its chunk of (token, slot) items.
+//   2. scan_kernel: one block turns the per-chunk histograms into expert
+//      offsets, padded (128-row) offsets and per-chunk base positions.
+//   3. scatter_kernel: each block ranks its chunk's items stably within each
+//      expert (warp match + warps in order) and writes the permutation.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteThreads = 256;
+
+struct RouteDims {
+  int T, E, k, chunk_tokens, n_chunks;
+};
+
+inline RouteDims route_dims(int T, int E, int k) {
+  RouteDims d;
+  d.T = T; d.E = E; d.k = k;
+  d.chunk_tokens = kRouteThreads / k;
+  if (d.chunk_tokens < 1) d.chunk_tokens = 1;
+  d.n_chunks = (T + d.chunk_tokens - 1) / d.chunk_tokens;
+  return d;
+}
+
+// Larger of two (value, index) candidates: higher value, then lower index.
+MOE_DEVINL bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+
+template <int NV>  // logits per lane: NV * 32 >= E
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, RouteDims d,
+                                                              int32_t* __restrict__ topk_id,
+                                                              float* __restrict__ topk_w,
+                                                              int32_t* __restrict__ chunk_counts) {
+  extern __shared__ int hist[];  // [E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * d.chunk_tokens;
+  const int t1 = min(d.T, t0 + d.chunk_tokens);
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+
+  for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
+    const float* row = logits + static_cast<int64_t>(t) * d.E;
+    float v[NV];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      int e = lane + 32 * i;
+      if (e < d.E) v[i] = __ldg(row + e);
+      else { v[i] = 0.0f; taken |= 1u << i; }
+    }
+    float my_v = 0.0f;
+    int my_i = 0;
+    for (int j = 0; j < d.k; ++j) {
+      float bv = -__int_as_float(0x7f800000);
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (!(taken >> i & 1u) && better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) { my_v = bv; my_i = bi; }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    float ex = (lane < d.k) ? route_exp(__fsub_rn(my_v, m)) : 0.0f;
+    float sum = 0.0f;
+    for (int j = 0; j < d.k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+    if (lane < d.k) {
+      int64_t o = static_cast<int64_t>(t) * d.k + lane;
+      topk_id[o] = my_i;
+      topk_w[o] = __fdiv_rn(ex, sum);
+      atomicAdd(&hist[my_i], 1);
+    }
+  }
+  __syncthreads();
+  int32_t* out = chunk_counts + static_cast<int64_t>(blockIdx.x) * d.E;
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) out[e] = hist[e];
+}
+
+// Exclusive scan of one value per thread over a block of up to 1024 threads.
+MOE_DEVINL int block_exclusive_scan(int v, int* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int nw = (blockDim.x + 31) >> 5;
+    int t = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < nw) warp_tot[lane] = t;  // inclusive warp prefix
+  }
+  __syncthreads();
+  int before = warp ? warp_tot[warp - 1] : 0;
+  int r = before + x - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(RouteDims d, int32_t* __restrict__ chunk_counts,
+                                                     int32_t* __restrict__ expert_offsets,
+                                                     int32_t* __restrict__ pad_offsets) {
+  __shared__ int warp_tot[32];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < d.E)
+    for (int b = 0; b < d.n_chunks; ++b) total += chunk_counts[static_cast<int64_t>(b) * d.E + e];
+  int off = block_exclusive_scan(e < d.E ? total : 0, warp_tot);
+  int padded = e < d.E ? ((total + 127) / 128) * 128 : 0;
+  int poff = block_exclusive_scan(padded, warp_tot);
+  if (e < d.E) {
+    expert_offsets[e] = off;
+    pad_offsets[e] = poff;
+    if (e == d.E - 1) {
+      expert_offsets[d.E] = off + total;
+      pad_offsets[d.E] = poff + padded;
+    }
+    int run = off;
+    for (int b = 0; b < d.n_chunks; ++b) {
+      int64_t o = static_cast<int64_t>(b) * d.E + e;
+      int c = chunk_counts[o];
+      chunk_counts[o] = run;  // becomes the chunk's first position for expert e
+      run += c;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) scatter_kernel(RouteDims d, const int32_t* __restrict__ topk_id,
+                                                                const int32_t* __restrict__ chunk_base,
+                                                                const int32_t* __restrict__ expert_offsets,
+                                                                const int32_t* __restrict__ pad_offsets,
+                                                                int32_t* __restrict__ perm_to_expanded,
+                                                                int32_t* __restrict__ expanded_to_perm,
+                                                                int32_t* __restrict__ expanded_to_row) {
+  extern __shared__ int cnt[];  // [E] items of each expert seen so far in this chunk
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * d.chunk_tokens * d.k;
+  const int64_t i1 = min(static_cast<int64_t>(d.T) * d.k, i0 + static_cast<int64_t>(d.chunk_tokens) * d.k);
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) cnt[e] = 0;
+  const int64_t i = i0 + threadIdx.x;
+  const bool valid = i < i1;
+  const int e = valid ? topk_id[i] : -1;
+  const unsigned active = __ballot_sync(0xffffffffu, valid);
+  unsigned peers = 0;
+  if (valid) peers = __match_any_sync(active, e);
+  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+  for (int w = 0; w < kRouteThreads / 32; ++w) {
+    __syncthreads();
+    if (warp == w && valid) {
+      int base = cnt[e];
+      __syncwarp(active);
+      int leader = __ffs(peers) - 1;
+      if (lane == leader) cnt[e] = base + __popc(peers);
+      int64_t p = static_cast<int64_t>(chunk_base[static_cast<int64_t>(blockIdx.x) * d.E + e]) + base + rank_in_warp;
+      perm_to_expanded[p] = static_cast<int32_t>(i);
+      expanded_to_perm[i] = static_cast<int32_t>(p);
+      expanded_to_row[i] = static_cast<int32_t>(pad_offsets[e] + (p - expert_offsets[e]));
+    }
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_route_permute_workspace_size(int T, int E, int k) {
+  if (T < 1 || E < 1 || k < 1) return 0;
+  RouteDims d = route_dims(T, E, k);
+  size_t counts = static_cast<size_t>(d.n_chunks) * E * sizeof(int32_t);
+  size_t pads = static_cast<size_t>(E + 1) * sizeof(int32_t);
+  return ((counts + 255) / 256) * 256 + ((pads + 255) / 256) * 256;
+}
+
+namespace moe {
+// Padded offsets live right after the chunk counts in the routing workspace.
+int32_t* route_pad_offsets(void* ws, int T, int E, int k) {
+  RouteDims d = route_dims(T, E, k);
+  size_t counts = static_cast<size_t>(d.n_chunks) * E * sizeof(int32_t);
+  return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + ((counts + 255) / 256) * 256);
+}
+}  // namespace moe
+
+extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* topk_id, float* topk_w,
+                                        int32_t* expert_offsets, int32_t* perm_to_expanded,
+                                        int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (!logits || !topk_id || !topk_w || !expert_offsets || !perm_to_expanded || !expanded_to_perm ||
+      !expanded_to_row)
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < moe_route_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteDims d = route_dims(T, E, k);
+  int32_t* counts = static_cast<int32_t*>(ws);
+  int32_t* pads = route_pad_offsets(ws, T, E, k);
+  const size_t hist_bytes = sizeof(int) * E;
+  const int nv = (E + 31) / 32;
+#define MOE_ROUTE(NV) route_kernel<NV><<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts)
+  if (nv <= 1) MOE_ROUTE(1);
+  else if (nv <= 2) MOE_ROUTE(2);
+  else if (nv <= 4) MOE_ROUTE(4);
+  else if (nv <= 8) MOE_ROUTE(8);
+  else if (nv <= 16) MOE_ROUTE(16);
+  else MOE_ROUTE(32);
+#undef MOE_ROUTE
+  scan_kernel<<<1, ((E + 31) / 32) * 32, 0, st>>>(d, counts, expert_offsets, pads);
+  scatter_kernel<<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(d, topk_id, counts, expert_offsets, pads,
+                                                                perm_to_expanded, expanded_to_perm, expanded_to_row);
+  return check_launch();
+}

@@ -1,0 +1,380 @@
+"""GPU parity of every kernel against the CPU oracle, through the C ABI.
+
+Integer and byte work (routing ids, router weights, permutation, NVFP4 codes
+and scales) must match bit for bit; GEMM, SiLU and FINALIZE outputs must stay
+within |gpu - ref| <= 1e-2 (|ref| + 1e-3 rms(ref)) elementwise.  Sizes span
+several tiles, ragged expert counts (0, 1, 31, 33, 128, 129, ...) and the
+partial last K tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_moe_grouped_gb300 as moe
+import oracle
+from nvfp4_moe_grouped_gb300 import inputs
+from tests._helpers import bf16_to_np, counts_to_offsets, padded_rows_of_items, tol_check, untile_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _tie_logits(T, E, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randint(0, 6, (T, E), generator=g).float() * 0.5).numpy()
+
+
+# ------------------------------------------------------------------ routing / permutation
+
+@pytest.mark.parametrize("T,E,k,kind", [(16, 8, 2, "normal"), (300, 256, 8, "normal"), (1024, 256, 8, "zipf"),
+                                        (5, 64, 3, "normal"), (1, 4, 4, "normal"), (777, 256, 8, "ties"),
+                                        (64, 1000, 32, "normal"), (4096, 256, 8, "normal")])
+def test_route_permute_bitexact(T, E, k, kind):
+    if kind == "zipf":
+        logits = inputs.router_logits(T, E, zipf_s=1.1).numpy()
+    elif kind == "ties":
+        logits = _tie_logits(T, E, 9)
+    else:
+        logits = inputs.router_logits(T, E, seed=T * 7 + E).numpy()
+    ids, w = oracle.route(logits, k)
+    offs, p2e, e2p = oracle.permute(ids, E)
+    r = moe.moe_route_permute(torch.from_numpy(logits).to(DEV), k)
+    torch.cuda.synchronize()
+    assert np.array_equal(r.topk_id.cpu().numpy(), ids)
+    assert np.array_equal(r.topk_w.cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r.expert_offsets.cpu().numpy(), offs)
+    assert np.array_equal(r.perm_to_expanded.cpu().numpy(), p2e)
+    assert np.array_equal(r.expanded_to_perm.cpu().numpy(), e2p)
+    rows = padded_rows_of_items(offs.astype(np.int64), ids.reshape(-1), e2p)
+    assert np.array_equal(r.expanded_to_row.cpu().numpy(), rows)
+
+
+def test_route_permute_is_deterministic():
+    T, E, k = 2048, 256, 8
+    logits = torch.from_numpy(inputs.router_logits(T, E, seed=5).numpy()).to(DEV)
+    a = moe.moe_route_permute(logits, k)
+    b = moe.moe_route_permute(logits, k)
+    for f in ("topk_id", "topk_w", "expert_offsets", "perm_to_expanded", "expanded_to_perm", "expanded_to_row"):
+        assert torch.equal(getattr(a, f), getattr(b, f)), f
+
+
+# ------------------------------------------------------------------ quantisation
+
+@pytest.mark.parametrize("rows,K", [(1, 16), (37, 256), (300, 6144), (128, 2048)])
+def test_quantize_linear_bf16_bitexact(rows, K):
+    x = inputs.activations(rows, K, seed=rows + K)
+    codes_ref, sf_ref, s_ref = oracle.quantize_dynamic(x.float().numpy())
+    codes, sf, s = moe.nvfp4_quantize(x.to(DEV))
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+    assert s.cpu().numpy()[0] == np.float32(s_ref)
+
+
+def test_quantize_static_scale_and_zero_rows():
+    x = inputs.activations(64, 512, seed=3).float()
+    x[5] = 0.0
+    x[7, :16] = 1e-30
+    s = 0.01
+    codes_ref, sf_ref = oracle.quantize(x.numpy(), s)
+    codes, sf, _ = moe.nvfp4_quantize(x.to(DEV), torch.tensor([s], dtype=torch.float32, device=DEV))
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+
+
+def test_quantize_weights_grouped_tiled_interleaved_bitexact():
+    E, N, K = 3, 256, 320
+    w = inputs.expert_weights(E, N, K, 77)
+    c_ref, s_ref, sc_ref = oracle.quantize_weights(w.numpy())
+    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(pw.scale.cpu().numpy(), sc_ref)
+    rowmap = moe.gate_up_row_map(N, "cpu").numpy()
+    codes = pw.codes.cpu().numpy()
+    for e in range(E):
+        assert np.array_equal(codes[e][rowmap], c_ref[e])
+        sf = untile_rows(pw.sf, e * N + rowmap, K)
+        assert np.array_equal(sf, s_ref[e])
+
+
+def test_quantize_gather_into_padded_tiled_rows():
+    T, E, k, H = 50, 16, 4, 256
+    x = inputs.activations(T, H, seed=4)
+    logits = inputs.router_logits(T, E, seed=8).numpy()
+    ids, _ = oracle.route(logits, k)
+    offs, p2e, e2p = oracle.permute(ids, E)
+    xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
+    rows = padded_rows_of_items(offs.astype(np.int64), ids.reshape(-1), e2p)
+    alloc = moe.padded_rows_max(T * k, E)
+    codes, sf, s = moe.nvfp4_quantize(x.to(DEV), None, n_items=T * k, src_div=k,
+                                      dst_row=torch.from_numpy(rows.astype(np.int32)).to(DEV),
+                                      sf_layout=moe.SF_TILED, dst_rows_alloc=alloc)
+    tok = np.arange(T * k) // k
+    assert np.array_equal(codes.cpu().numpy()[rows], xc[tok])
+    assert np.array_equal(untile_rows(sf, rows, H), xs[tok])
+    assert s.item() == np.float32(xsc)
+
+
+# ------------------------------------------------------------------ finalize
+
+@pytest.mark.parametrize("T,k,N", [(16, 2, 256), (333, 8, 1024), (1, 1, 8)])
+def test_finalize_matches_oracle(T, k, N):
+    R = T * k
+    g = torch.Generator().manual_seed(T + N)
+    y = torch.randn(R + 7, N, generator=g).to(torch.bfloat16)
+    w = torch.rand(T, k, generator=g)
+    w = w / w.sum(1, keepdim=True)
+    rows = torch.randperm(R + 7, generator=g)[:R].to(torch.int32)
+    ref = oracle.finalize(bf16_to_np(y), w.numpy(), rows.numpy())
+    out = moe.moe_finalize(y.to(DEV), w.to(DEV), rows.to(DEV))
+    tol_check(bf16_to_np(out), ref, "finalize")
+
+
+# ------------------------------------------------------------------ grouped GEMM
+
+def _routed_operand(x_bf16, offs):
+    """Quantise routed rows (unpadded, expert-grouped) into the padded tiled layout on the GPU."""
+    R = x_bf16.shape[0]
+    pad = oracle.padded_offsets(offs)
+    e_of_row = np.repeat(np.arange(len(offs) - 1), np.diff(offs))
+    dst = (pad[e_of_row] + (np.arange(R) - offs[e_of_row])).astype(np.int32)
+    alloc = max(128, int(pad[-1]))
+    alloc = ((alloc + 127) // 128) * 128
+    codes, sf, s = moe.nvfp4_quantize(x_bf16.to(DEV), None, dst_row=torch.from_numpy(dst).to(DEV),
+                                      sf_layout=moe.SF_TILED, dst_rows_alloc=alloc)
+    return codes, sf, s, dst
+
+
+GEMM_CASES = [
+    ([3, 0, 17, 9], 128, 256),
+    ([32] * 8, 256, 512),
+    ([1, 31, 33, 64, 65, 128, 129, 200, 0, 255], 256, 320),
+    ([40, 7], 384, 128),
+    ([300], 128, 1024),
+]
+
+
+@pytest.mark.parametrize("counts,N,K", GEMM_CASES)
+def test_grouped_gemm_none_matches_oracle(counts, N, K):
+    E = len(counts)
+    offs = counts_to_offsets(counts)
+    R = int(offs[-1])
+    x = inputs.activations(R, K, seed=R + K)
+    w = inputs.expert_weights(E, N, K, 100 + N)
+    xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
+    wq = oracle.quantize_weights(w.numpy())
+    ref = oracle.grouped_gemm(xc, xs, xsc, *wq, offs, N, K)
+    codes, sf, s, dst = _routed_operand(x, offs)
+    assert np.array_equal(codes.cpu().numpy()[dst], xc)
+    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=False)
+    out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV), moe.EPI_NONE)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    tol_check(bf16_to_np(out)[dst], ref, "grouped GEMM NONE")
+
+
+def test_grouped_gemm_identity_expert_is_exact():
+    """W = identity (e2m1 1.0, scales 1), inputs on the e2m1 grid: the output is the input, exactly."""
+    K = N = 256
+    R = 40
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    rng = np.random.default_rng(1)
+    x = grid[rng.integers(0, 8, (R, K))] * rng.choice([-1, 1], (R, K)).astype(np.float32)
+    x[:, ::16] = 6.0  # every block's amax is the tensor amax: block scale 448, codes = x
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    xf = xt.float().numpy()
+    codes, sf, s, dst = _routed_operand(xt, counts_to_offsets([R]))
+    eye = torch.eye(K, dtype=torch.float32)[None] * 1.0
+    pw = moe.prepare_expert_weights(eye.to(DEV), gate_up=False)
+    out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(counts_to_offsets([R])).to(DEV))
+    got = bf16_to_np(out)[dst]
+    xc, xs, xsc = oracle.quantize_dynamic(xf)
+    wq = oracle.quantize_weights(eye.numpy())
+    ref = oracle.grouped_gemm(xc, xs, xsc, *wq, counts_to_offsets([R]), N, K)
+    assert np.allclose(ref, xf, rtol=1e-6, atol=0)  # exact up to the FP32 rounding of the scales
+    assert np.array_equal(got, xf.astype(np.float64))
+
+
+def _assert_rare_adjacent_flips(got, ref):
+    """Decoded NVFP4 values of a requantised FP32 tensor whose FP32 inputs differ by rounding:
+    a value may differ only near a rounding boundary (rare) and then by at most one e2m1 step
+    of its block (2/6 of the block maximum, plus the e4m3 scale's own rounding)."""
+    mism = got != ref
+    assert mism.mean() < 2e-3, mism.mean()
+    if mism.any():
+        blk = np.abs(ref).reshape(ref.shape[0], -1, 16).max(-1)
+        bound = np.repeat(blk, 16, axis=1) * (2.0 / 6.0) * 1.07 + 1e-30
+        assert np.all(np.abs(got - ref)[mism] <= bound[mism])
+    return mism
+
+
+def _silu_case(counts, I, H, seed):
+    E = len(counts)
+    offs = counts_to_offsets(counts)
+    R = int(offs[-1])
+    x = inputs.activations(R, H, seed=seed)
+    w13 = inputs.expert_weights(E, 2 * I, H, seed + 1)
+    xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
+    w13q = oracle.quantize_weights(w13.numpy())
+    y1 = oracle.grouped_gemm(xc, xs, xsc, *w13q, offs, 2 * I, H)
+    h = oracle.silu_mul(y1)
+    h_scale = oracle.tensor_scale_from_amax(oracle.amax(h.astype(np.float32)))
+    return offs, x, w13, h, h_scale
+
+
+@pytest.mark.parametrize("counts,I,H", [([3, 0, 17, 9], 64, 256), ([1, 33, 129, 64], 128, 320), ([32] * 4, 256, 512)])
+def test_grouped_gemm_silu_mul_quant(counts, I, H):
+    offs, x, w13, h_ref, h_scale = _silu_case(counts, I, H, 11 + I)
+    codes, sf, s, dst = _routed_operand(x, offs)
+    pw = moe.prepare_expert_weights(w13.to(DEV), gate_up=True)
+    alloc = codes.shape[0]
+    h_f32 = torch.zeros(alloc, I, dtype=torch.float32, device=DEV)
+    hs_out = torch.zeros(1, dtype=torch.float32, device=DEV)
+    hc, hsf = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV), moe.EPI_SILU_MUL_QUANT,
+                                         h_scale=h_scale, h_f32=h_f32, h_scale_out=hs_out)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    assert hs_out.item() == np.float32(h_scale)
+    # (i) the FP32 SiLU-mul output against the oracle's FP64 one
+    tol_check(h_f32.cpu().numpy()[dst], h_ref, "SiLU-mul h")
+    # (ii) the requantised codes: the oracle's own codes of its own h, compared
+    # as decoded values; a code may differ only where h sits on a rounding
+    # boundary, by one grid step, and such flips must be rare.
+    hc_ref, hs_ref = oracle.quantize(h_ref.astype(np.float32), h_scale)
+    got = oracle.dequantize(hc.cpu().numpy()[dst], untile_rows(hsf, dst, I))
+    ref = oracle.dequantize(hc_ref, hs_ref)
+    _assert_rare_adjacent_flips(got, ref)
+
+
+def test_grouped_gemm_silu_quant_exact_inputs():
+    """Large gate values make silu(g) = g exactly in FP32, and gate/up products are exact, so the
+    requantised codes and scales are fully determined: compare them bit for bit."""
+    I, H, R = 64, 256, 48
+    E = 1
+    # x row r: 1.0 in column (r % 4) * 64, zero elsewhere -> Y[r][n] = W[n][(r%4)*64]
+    x = torch.zeros(R, H)
+    for r in range(R):
+        x[r, (r % 4) * 64] = 1.0
+    rng = np.random.default_rng(5)
+    w = np.zeros((1, 2 * I, H), np.float32)
+    for c in range(4):
+        w[0, :I, c * 64] = rng.choice([32.0, 48.0, 64.0, 96.0], I)         # gate: silu(g) = g exactly
+        w[0, I:, c * 64] = rng.choice([-3.0, -1.0, 0.5, 1.5, 2.0, 6.0], I)   # up
+    wt = torch.from_numpy(w)
+    offs = counts_to_offsets([R])
+    xc, xs, xsc = oracle.quantize_dynamic(x.numpy())
+    wq = oracle.quantize_weights(w)
+    y1 = oracle.grouped_gemm(xc, xs, xsc, *wq, offs, 2 * I, H)
+    h = oracle.silu_mul(y1)
+    assert np.all(h.astype(np.float32) == h)  # exact in FP32
+    h_scale = oracle.tensor_scale_from_amax(oracle.amax(h.astype(np.float32)))
+    hc_ref, hs_ref = oracle.quantize(h.astype(np.float32), h_scale)
+    codes, sf, s, dst = _routed_operand(x.to(torch.bfloat16), offs)
+    pw = moe.prepare_expert_weights(wt.to(DEV), gate_up=True)
+    h_f32 = torch.zeros(codes.shape[0], I, dtype=torch.float32, device=DEV)
+    hc, hsf = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV), moe.EPI_SILU_MUL_QUANT,
+                                         h_scale=h_scale, h_f32=h_f32)
+    torch.cuda.synchronize()
+    assert np.array_equal(h_f32.cpu().numpy()[dst], h.astype(np.float32))
+    assert np.array_equal(hc.cpu().numpy()[dst], hc_ref)
+    assert np.array_equal(untile_rows(hsf, dst, I), hs_ref)
+
+
+@pytest.mark.parametrize("T,E,k,H,I", [(16, 8, 2, 256, 128), (200, 32, 4, 384, 256), (64, 256, 8, 256, 64)])
+def test_grouped_gemm_finalize_matches_oracle(T, E, k, H, I):
+    logits = inputs.router_logits(T, E, seed=T + E).numpy()
+    ids, w = oracle.route(logits, k)
+    offs, p2e, e2p = oracle.permute(ids, E)
+    R = T * k
+    g = torch.Generator().manual_seed(T)
+    h = (torch.randn(R, I, generator=g) * 0.3).numpy()
+    hc, hs, hsc = oracle.quantize_dynamic(h)
+    w2 = inputs.expert_weights(E, H, I, 500)
+    w2q = oracle.quantize_weights(w2.numpy())
+    y2 = oracle.grouped_gemm(hc, hs, hsc, *w2q, offs, H, I)
+    ref = oracle.finalize(y2, w, e2p)
+    # GPU: the oracle's h (FP32 values) quantised on the GPU into padded rows
+    codes, sf, s, dst = _routed_operand(torch.from_numpy(h), offs.astype(np.int64))
+    assert np.array_equal(codes.cpu().numpy()[dst], hc)
+    pw = moe.prepare_expert_weights(w2.to(DEV), gate_up=False)
+    out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV), moe.EPI_FINALIZE,
+                                     perm_to_expanded=torch.from_numpy(p2e).to(DEV),
+                                     topk_w=torch.from_numpy(w).to(DEV), T=T, k=k)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    tol_check(bf16_to_np(out), ref, "FINALIZE")
+
+
+# ------------------------------------------------------------------ fused layer
+
+def _layer_case(T, E, k, H, I, zipf=None):
+    x = inputs.activations(T, H)
+    logits = inputs.router_logits(T, E, zipf_s=zipf)
+    w13f = inputs.expert_weights(E, 2 * I, H, inputs.gate_up_seed_base())
+    w2f = inputs.expert_weights(E, H, I, inputs.down_seed_base(E))
+    return x, logits, w13f, w2f
+
+
+@pytest.mark.parametrize("T,E,k,H,I,zipf", [(16, 8, 2, 256, 128, None), (96, 64, 6, 512, 192, None),
+                                            (128, 32, 4, 256, 128, 1.1)])
+def test_moe_forward_matches_oracle(T, E, k, H, I, zipf):
+    x, logits, w13f, w2f = _layer_case(T, E, k, H, I, zipf)
+    w13 = oracle.quantize_weights(w13f.numpy())
+    w2 = oracle.quantize_weights(w2f.numpy())
+    ref = oracle.moe_layer(x.float().numpy(), logits.numpy(), w13, w2, k)
+    h_scale = float(oracle.tensor_scale_from_amax(oracle.amax(ref.h.astype(np.float32))))
+    pw13 = moe.prepare_expert_weights(w13f.to(DEV), gate_up=True)
+    pw2 = moe.prepare_expert_weights(w2f.to(DEV), gate_up=False)
+    fwd = moe.MoeForward(T, E, k, H, I)
+    out = fwd(x.to(DEV), logits.to(DEV), pw13, pw2, h_scale)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    R = T * k
+    # routing, permutation and the quantised activations: bit-exact
+    assert np.array_equal(fwd.view("topk_id", torch.int32, (T, k)).cpu().numpy(), ref.topk_id)
+    assert np.array_equal(fwd.view("topk_w", torch.float32, (T, k)).cpu().numpy(), ref.topk_w)
+    assert np.array_equal(fwd.view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy(), ref.expert_offsets)
+    assert np.array_equal(fwd.view("perm_to_expanded", torch.int32, (R,)).cpu().numpy(), ref.perm_to_expanded)
+    rows = padded_rows_of_items(ref.expert_offsets.astype(np.int64), ref.topk_id.reshape(-1), ref.expanded_to_perm)
+    P = fwd.layout.padded_rows
+    xcodes = fwd.view("x_codes", torch.uint8, (P, H // 2)).cpu().numpy()
+    perm_rows = rows[ref.perm_to_expanded]
+    assert np.array_equal(xcodes[perm_rows], ref.x_codes)
+    assert np.array_equal(untile_rows(fwd.view("x_sf", torch.uint8, (P * H // 16,)), perm_rows, H), ref.x_sf)
+    # the requantised intermediate: rare one-step flips only
+    hcodes = fwd.view("h_codes", torch.uint8, (P, I // 2)).cpu().numpy()[perm_rows]
+    hsf = untile_rows(fwd.view("h_sf", torch.uint8, (P * I // 16,)), perm_rows, I)
+    href_c, href_s = oracle.quantize(ref.h.astype(np.float32), h_scale)
+    flips = _assert_rare_adjacent_flips(oracle.dequantize(hcodes, hsf), oracle.dequantize(href_c, href_s))
+    got = bf16_to_np(out)
+    rel = np.linalg.norm(got - ref.out) / np.linalg.norm(ref.out)
+    assert rel < 1e-2, rel
+    if not flips.any():
+        tol_check(got, ref.out, "moe_forward")
+
+
+def test_timeout_path_reports_and_recovers():
+    """A pipeline stage that is never filled: the bounded waits give up, the kernel reports
+    MOE_ERR_TIMEOUT and returns; the context stays usable."""
+    counts, N, K = [32, 32], 128, 512
+    offs = counts_to_offsets(counts)
+    x = inputs.activations(64, K, seed=1)
+    w = inputs.expert_weights(2, N, K, 3)
+    codes, sf, s, dst = _routed_operand(x, offs)
+    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=False)
+    torch.cuda.synchronize()
+    moe.device_error()
+    moe.set_wait_timeout_ns(50_000_000)
+    moe.debug_set_flags(1)
+    try:
+        moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV))
+        code, where = moe.device_error()
+    finally:
+        moe.debug_set_flags(0)
+        moe.set_wait_timeout_ns(0)
+    assert code == 6  # MOE_ERR_TIMEOUT
+    out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV))
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
+    ref = oracle.grouped_gemm(xc, xs, xsc, *oracle.quantize_weights(w.numpy()), offs, N, K)
+    tol_check(bf16_to_np(out)[dst], ref, "after timeout")
