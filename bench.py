@@ -1,0 +1,546 @@
+"""Benchmark of the NVFP4 MoE layer on GB300.
+
+One step = the whole layer over one batch: route + permute, quantise x into
+the routed rows, gate_up grouped GEMM with SiLU-mul + requantisation, down
+grouped GEMM with FINALIZE.  Default workload: the full decode layer with
+T=1024 tokens, E=256 experts, top-8, H=6144, I=2048 (uniform router logits).
+
+value: tokens/s of the layer with inputs resident in HBM (CUDA events on the
+launching stream over exactly --steps steps, after --warmup steps).  The
+expert weights (5.4 GB of NVFP4) are far larger than L2 (129 MB), so every
+step streams them from HBM; no L2 flush is needed.
+e2e: the same through moe_forward with pinned host buffers: every step copies
+x and the logits to the device and the output back.
+roofline: the gate_up grouped GEMM (the largest kernel), algorithmic bytes per
+launch / its event-timed duration, against the measured HBM copy bandwidth.
+cpu_baseline: the CPU oracle on a bounded sample of the same batch.
+
+--impl reference times the CPU oracle (the reference arm of this repo) on a
+bounded sample of the same workload and prints the same JSON line shape.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_DEF, E_DEF, K_DEF, H_DEF, I_DEF = 1024, 256, 8, 6144, 2048
+METRIC = "MoE-layer tokens/s and grouped-GEMM TFLOPS & HBM GB/s vs roofline, 1 GB300"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=T_DEF)
+    ap.add_argument("--zipf", type=float, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="layer", choices=["layer", "gemm"],
+                    help="layer: the full MoE layer (default); gemm: one grouped GEMM, 256 experts x 32 rows, "
+                         "K=6144, N=2048, NONE epilogue")
+    ap.add_argument("--profile-steps", action="store_true",
+                    help="no JSON; only the steps run between cudaProfilerStart/Stop (for ncu)")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1952.0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ setup
+
+def make_layer(T, E, k, H, I, zipf, dev):
+    import nvfp4_moe_grouped_gb300 as moe
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    x = inputs.activations(T, H)                       # CPU generator, seed 0
+    logits = inputs.router_logits(T, E, zipf_s=zipf)   # CPU generator, seed 1
+    # full-size weights: drawn on the device with the per-expert seeds, quantised there
+    w13f = inputs.expert_weights(E, 2 * I, H, inputs.gate_up_seed_base(), device=dev)
+    pw13 = moe.prepare_expert_weights(w13f, gate_up=True)
+    del w13f
+    w2f = inputs.expert_weights(E, H, I, inputs.down_seed_base(E), device=dev)
+    pw2 = moe.prepare_expert_weights(w2f, gate_up=False)
+    del w2f
+    torch.cuda.empty_cache()
+    return x, logits, pw13, pw2
+
+
+def calibrate_h_scale(fwd, xd, ld, pw13):
+    """Static decode multiplier of the intermediate: amax of this batch's h / (6*448)."""
+    import nvfp4_moe_grouped_gb300 as moe
+    L = fwd.layout
+    T, E, k, H, I = fwd.T, fwd.E, fwd.k, fwd.H, fwd.I
+    P = L.padded_rows
+    r = moe.moe_route_permute(ld, k)
+    codes, sf, s = moe.nvfp4_quantize(xd, None, n_items=T * k, src_div=k, dst_row=r.expanded_to_row,
+                                      sf_layout=moe.SF_TILED, dst_rows_alloc=P)
+    h_f32 = torch.zeros(P, I, dtype=torch.float32, device=xd.device)
+    moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw13, r.expert_offsets, moe.EPI_SILU_MUL_QUANT, h_scale=1.0, h_f32=h_f32)
+    amax = float(h_f32.abs().max().item())
+    del h_f32, codes, sf
+    return amax / 2688.0 if amax > 0 else 1.0
+
+
+def algorithmic_bytes(expert_counts, T, k, H, I):
+    """Bytes the layer must move: weights of active experts once, activations, intermediates, outputs."""
+    active = int((expert_counts > 0).sum())
+    R = T * k
+    w13 = 2 * I * H // 2 + 2 * I * H // 16
+    w2 = H * I // 2 + H * I // 16
+    gate_up = active * w13 + R * (H // 2 + H // 16) + R * (I // 2 + I // 16)
+    down = active * w2 + R * (I // 2 + I // 16) + T * H * 4 * 2   # FP32 accumulate (read-modify-write)
+    layer = gate_up + down + T * H * 2 + T * E * 4 + T * H * 2
+    return {"gate_up": gate_up, "down": down, "layer": layer, "active_experts": active}
+
+
+# ------------------------------------------------------------------ CPU oracle sample
+
+def oracle_sample(x, logits, T, E, k, H, I, n_tokens, h_scale, dev):
+    """Time the CPU oracle on the first n_tokens tokens of the batch (weights of their experts only)."""
+    import oracle
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    xs = x[:n_tokens].float().numpy()
+    ls = logits[:n_tokens].numpy()
+    ids, _ = oracle.route(ls, k)
+    experts = sorted(set(ids.reshape(-1).tolist()))
+    wq13, wq2 = {}, {}
+    for e in experts:   # untimed: model preparation (the FP32 weights are redrawn with the same seeds)
+        w13 = inputs.expert_weight(e, 2 * I, H, inputs.gate_up_seed_base(), device=dev).cpu().numpy()
+        w2 = inputs.expert_weight(e, H, I, inputs.down_seed_base(E), device=dev).cpu().numpy()
+        wq13[e] = oracle.quantize_dynamic(w13)
+        wq2[e] = oracle.quantize_dynamic(w2)
+    t0 = time.perf_counter()
+    # the layer in the method's order, restricted to the sampled tokens; the activations' tensor
+    # scale is the whole batch's
+    ids, w = oracle.route(ls, k)
+    xsc = oracle.tensor_scale_from_amax(oracle.amax(x.float().numpy()))
+    xc, xsf = oracle.quantize(xs, xsc)
+    out = np.zeros((n_tokens, H))
+    for t in range(n_tokens):
+        for j in range(k):
+            e = int(ids[t, j])
+            c13, s13, sc13 = wq13[e]
+            y1 = oracle.grouped_gemm(xc[t:t + 1], xsf[t:t + 1], xsc, c13[None], s13[None],
+                                     np.array([sc13], np.float32), np.array([0, 1], np.int32), 2 * I, H)
+            h = oracle.silu_mul(y1).astype(np.float32)
+            hc, hs = oracle.quantize(h, h_scale)
+            c2, s2, sc2 = wq2[e]
+            y2 = oracle.grouped_gemm(hc, hs, h_scale, c2[None], s2[None], np.array([sc2], np.float32),
+                                     np.array([0, 1], np.int32), H, I)
+            out[t] += float(w[t, j]) * y2[0]
+    dt = time.perf_counter() - t0
+    return dt, out
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: bounded samples of the same workload."""
+    if rank != 0:
+        return
+    T, E, k, H, I = args.tokens, E_DEF, K_DEF, H_DEF, I_DEF
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    from nvfp4_moe_grouped_gb300 import inputs
+    x = inputs.activations(T, H)
+    logits = inputs.router_logits(T, E, zipf_s=args.zipf)
+    n_tok = 1
+    h_scale = 0.01
+    for _ in range(args.warmup):
+        oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev)
+    times = []
+    for _ in range(args.steps):
+        dt, _ = oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev)
+        times.append(dt)
+    tot = sum(times)
+    value = n_tok * args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"moe_layer_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf else ""),
+                       "sample": f"{n_tok} token(s) of the batch per step"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{n_tok} token(s) per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import nvfp4_moe_grouped_gb300 as moe
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T, E, k, H, I = args.tokens, E_DEF, K_DEF, H_DEF, I_DEF
+    x, logits, pw13, pw2 = make_layer(T, E, k, H, I, args.zipf, dev)
+    xd, ld = x.to(dev), logits.to(dev)
+    fwd = moe.MoeForward(T, E, k, H, I, dev)
+    h_scale = calibrate_h_scale(fwd, xd, ld, pw13)
+    L = fwd.layout
+    P = L.padded_rows
+    R = T * k
+    stream = torch.cuda.current_stream()
+
+    # stage views inside the forward workspace (the same buffers moe_forward uses)
+    topk_id = fwd.view("topk_id", torch.int32, (T, k))
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+    def step(ev=None):
+        # the layer as its four C-ABI stages; events between them time each stage on this stream
+        r = route_into(fwd)
+        if ev is not None:
+            ev[0].record(stream)
+        quant_into(fwd, xd)
+        if ev is not None:
+            ev[1].record(stream)
+        gate_up_into(fwd, pw13, h_scale)
+        if ev is not None:
+            ev[2].record(stream)
+        down_into(fwd, pw2, out)
+        if ev is not None:
+            ev[3].record(stream)
+        return r
+
+    def route_into(f):
+        _call("moe_route_permute", f.lib.moe_route_permute(
+            _p(ld), T, E, k, f.ptr("topk_id"), f.ptr("topk_w"), f.ptr("expert_offsets"), f.ptr("perm_to_expanded"),
+            f.ptr("expanded_to_perm"), f.ptr("expanded_to_row"), f.ptr("route_ws"),
+            f.lib.moe_route_permute_workspace_size(T, E, k), _s()))
+
+    def quant_into(f, xdev):
+        _call("nvfp4_quantize", f.lib.nvfp4_quantize(
+            _p(xdev), 0, T, H, 1, f.ptr("x_scale"), 1, R, k, f.ptr("expanded_to_row"), f.ptr("x_codes"),
+            f.ptr("x_sf"), 1, P, f.ptr("quant_ws"), f.lib.nvfp4_quantize_workspace_size(1), _s()))
+
+    def gate_up_into(f, w, hs):
+        ep = moe.EpilogueArgs()
+        ep.h_scale = hs
+        ep.h_scale_out = f.ptr("h_scale")
+        ep.h_codes = f.ptr("h_codes")
+        ep.h_sf = f.ptr("h_sf")
+        _call("moe_grouped_gemm_nvfp4", f.lib.moe_grouped_gemm_nvfp4(
+            f.ptr("x_codes"), f.ptr("x_sf"), f.ptr("x_scale"), _p(w.codes), _p(w.sf), _p(w.scale),
+            f.ptr("expert_offsets"), E, P, 2 * I, H, moe.EPI_SILU_MUL_QUANT, _byref(ep), None, None, 0, _s()))
+
+    def down_into(f, w, o):
+        ep = moe.EpilogueArgs()
+        ep.perm_to_expanded = f.ptr("perm_to_expanded")
+        ep.topk_w = f.ptr("topk_w")
+        ep.T = T
+        ep.k = k
+        wsb = f.lib.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, T, H)
+        _call("moe_grouped_gemm_nvfp4", f.lib.moe_grouped_gemm_nvfp4(
+            f.ptr("h_codes"), f.ptr("h_sf"), f.ptr("h_scale"), _p(w.codes), _p(w.sf), _p(w.scale),
+            f.ptr("expert_offsets"), E, P, H, I, moe.EPI_FINALIZE, _byref(ep), _p(o), f.ptr("gemm_ws"), wsb, _s()))
+
+    import ctypes
+
+    def _p(t):
+        return ctypes.c_void_p(t.data_ptr())
+
+    def _s():
+        return ctypes.c_void_p(stream.cuda_stream)
+
+    def _byref(s):
+        return ctypes.byref(s)
+
+    def _call(name, st):
+        if st != 0:
+            raise moe.MoeError(name, st)
+
+    fwd.lib = moe._lib.load()
+    fwd.ptr = lambda name: ctypes.c_void_p(fwd.ws.data_ptr() + getattr(L, name))
+
+    if args.profile_steps:
+        for _ in range(max(1, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStart()
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        return
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    counts = np.diff(fwd.view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy())
+    ab = algorithmic_bytes(counts, T, k, H, I)
+
+    # ---- device-timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(stop)
+    prev = [start] + [evs[i][3] for i in range(args.steps - 1)]
+    stage_ms = np.zeros(4)
+    for i in range(args.steps):
+        stage_ms[0] += prev[i].elapsed_time(evs[i][0])
+        for j in range(1, 4):
+            stage_ms[j] += evs[i][j - 1].elapsed_time(evs[i][j])
+    stage_ms /= args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * T / (ms_step / 1e3)
+
+    # ---- end to end through moe_forward with pinned host buffers
+    xh = x.pin_memory()
+    lh = logits.pin_memory()
+    oh = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    xd2 = torch.empty_like(xd)
+    ld2 = torch.empty_like(ld)
+    out2 = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+    def e2e_step():
+        xd2.copy_(xh, non_blocking=True)
+        ld2.copy_(lh, non_blocking=True)
+        fwd(xd2, ld2, pw13, pw2, h_scale, out=out2)
+        oh.copy_(out2, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * T * args.steps / (e2e_ms / 1e3)
+
+    code, where = moe.device_error()
+    if code != 0:
+        raise RuntimeError(f"device error {code} at {where} during the benchmark")
+    if rank != 0:
+        return
+
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    gate_up_ms = stage_ms[2]
+    achieved = ab["gate_up"] / (gate_up_ms / 1e3) / 1e9
+    flops_gate_up = 2.0 * T * k * 2 * I * H
+    flops_layer = 2.0 * T * k * (2 * I * H + H * I)
+    traffic = None
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_tok = 2
+        dt, _ = oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev)
+        cpu = {"value": n_tok / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"the first {n_tok} tokens of the batch (their {n_tok * k} expert rows), one pass"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1xe2m1->f32", "data": "synthetic",
+        "config": {"workload": f"moe_layer_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf else "_uniform"),
+                   "tokens": T, "experts": E, "top_k": k, "hidden": H, "intermediate": I,
+                   "l2": "weights (5.4 GB) exceed L2; no flush", "parallelism": f"replicas{world}"},
+        "roofline": {"bound": "hbm", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": ab["gate_up"], "launch_ms": gate_up_ms},
+        "stages_ms": {"route_permute": stage_ms[0], "quantize_x": stage_ms[1], "gate_up_gemm": stage_ms[2],
+                      "down_gemm_finalize": stage_ms[3]},
+        "gemm_tflops": {"gate_up": flops_gate_up / (gate_up_ms / 1e3) / 1e12,
+                        "down": 2.0 * T * k * H * I / (stage_ms[3] / 1e3) / 1e12,
+                        "layer": flops_layer / (ms_step / 1e3) / 1e12},
+        "hbm_gbs_layer": ab["layer"] / (ms_step / 1e3) / 1e9,
+        "active_experts": ab["active_experts"],
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
+                "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": 9 * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gemm(args, rank, world, local_rank):
+    """One grouped GEMM at the decode shape: 256 experts x exactly 32 rows, K=6144, N=2048, NONE."""
+    import nvfp4_moe_grouped_gb300 as moe
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    E, rows, N, K = 256, 32, 2048, 6144
+    R = E * rows
+    offs = torch.arange(0, R + 1, rows, dtype=torch.int32)
+    pad = torch.arange(0, E + 1, dtype=torch.int64) * 128
+    dst = (pad[:-1, None] + torch.arange(rows)[None, :]).reshape(-1).to(torch.int32)
+    x = inputs.activations(R, K)
+    codes, sf, s = moe.nvfp4_quantize(x.to(dev), None, dst_row=dst.to(dev), sf_layout=moe.SF_TILED,
+                                      dst_rows_alloc=E * 128)
+    wf = inputs.expert_weights(E, N, K, 100, device=dev)
+    pw = moe.prepare_expert_weights(wf, gate_up=False)
+    del wf
+    torch.cuda.empty_cache()
+    offs_d = offs.to(dev)
+    out = torch.zeros(E * 128, N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, offs_d, moe.EPI_NONE, out=out)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if args.profile_steps:
+        torch.cuda.cudart().cudaProfilerStart()
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        return
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    w_bytes = E * N * (K // 2 + K // 16)
+    alg = w_bytes + R * (K // 2 + K // 16) + R * N * 2
+    flops = 2.0 * R * N * K
+    hbm_peak, _, peak_kind = peaks()
+    gbs = alg / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "grouped-GEMM TFLOPS & HBM GB/s vs roofline (NVFP4, NONE epilogue)", "value": gbs,
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1xe2m1->f32",
+            "data": "synthetic",
+            "config": {"workload": "grouped_gemm_E256_rows32_K6144_N2048_none",
+                       "l2": "weights (1.81 GB) exceed L2; no flush"},
+            "tflops": flops / (ms / 1e3) / 1e12,
+            "roofline": {"bound": "hbm", "kernel": "grouped_gemm NONE", "achieved": gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg, "launch_ms": ms},
+            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    try:
+        if args.workload == "gemm":
+            run_gemm(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -246,23 +246,28 @@ def test_grouped_gemm_silu_mul_quant(counts, I, H):
 
 
 def test_grouped_gemm_silu_quant_exact_inputs():
-    """Large gate values make silu(g) = g exactly in FP32, and gate/up products are exact, so the
-    requantised codes and scales are fully determined: compare them bit for bit."""
+    """Inputs chosen so every value on the way is exact in FP32 and FP64: power-of-two tensor
+    scales (amax = 2688 * 2^j), e4m3-exact block scales, gate values so large that silu(g) = g in
+    both precisions, products of 441 * 2^a.  The requantised codes and scales are then fully
+    determined: compare them bit for bit."""
     I, H, R = 64, 256, 48
-    E = 1
-    # x row r: 1.0 in column (r % 4) * 64, zero elsewhere -> Y[r][n] = W[n][(r%4)*64]
+    # x row r: 10.5 (= 2688 * 2^-8) in column (r % 4) * 64, zero elsewhere
     x = torch.zeros(R, H)
     for r in range(R):
-        x[r, (r % 4) * 64] = 1.0
+        x[r, (r % 4) * 64] = 10.5
     rng = np.random.default_rng(5)
+    mags = np.array([21.0, 42.0, 84.0, 168.0], np.float32)   # 168 = 2688 * 2^-4; block scales 56..448
     w = np.zeros((1, 2 * I, H), np.float32)
     for c in range(4):
-        w[0, :I, c * 64] = rng.choice([32.0, 48.0, 64.0, 96.0], I)         # gate: silu(g) = g exactly
-        w[0, I:, c * 64] = rng.choice([-3.0, -1.0, 0.5, 1.5, 2.0, 6.0], I)   # up
+        w[0, :I, c * 64] = rng.choice(mags, I)                                  # gate > 0: silu(g) = g
+        w[0, I:, c * 64] = rng.choice(mags, I) * rng.choice([-1.0, 1.0], I)     # up
+    w[0, 0, 0] = 168.0
     wt = torch.from_numpy(w)
     offs = counts_to_offsets([R])
     xc, xs, xsc = oracle.quantize_dynamic(x.numpy())
+    assert xsc == 2.0 ** -8
     wq = oracle.quantize_weights(w)
+    assert wq[2][0] == 2.0 ** -4
     y1 = oracle.grouped_gemm(xc, xs, xsc, *wq, offs, 2 * I, H)
     h = oracle.silu_mul(y1)
     assert np.all(h.astype(np.float32) == h)  # exact in FP32
