@@ -156,7 +156,7 @@ def calibrate_h_scale(fwd, xd, ld, pw13):
     return amax / 2688.0 if amax > 0 else 1.0
 
 
-def algorithmic_bytes(expert_counts, T, k, H, I):
+def algorithmic_bytes(expert_counts, T, E, k, H, I):
     """Bytes the layer must move: weights of active experts once, activations, intermediates, outputs."""
     active = int((expert_counts > 0).sum())
     R = T * k
@@ -348,7 +348,7 @@ def run_ours(args, rank, world, local_rank):
         step()
     torch.cuda.synchronize()
     counts = np.diff(fwd.view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy())
-    ab = algorithmic_bytes(counts, T, k, H, I)
+    ab = algorithmic_bytes(counts, T, E, k, H, I)
 
     # ---- device-timed region
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
