@@ -48,10 +48,20 @@
  *     by expert; expert e owns rows [P_e, P_e + M_e) where M_e is its count
  *     and P_e = sum over e' < e of ceil(M_e' / 128) * 128.  The rows between
  *     P_e + M_e and P_{e+1} are padding: never read into any result.
- *   Prepared expert weights: codes [E][N][K/2] and tiled scales over E*N rows
- *     (N % 128 == 0).  For the gate_up weights (N = 2I) the rows are
- *     interleaved in blocks of 64: prepared row 128*b + j is gate row 64*b + j
- *     and prepared row 128*b + 64 + j is up row 64*b + j (j < 64).
+ *   Blocked weights (what the GEMM reads for the expert weights; written by
+ *     nvfp4_quantize with MOE_SF_BLOCKED): the E*N weight rows (N % 128 == 0)
+ *     in 128-row tiles and K in 256-element tiles; tile (row tile t, K tile
+ *     kt) is one 18432-byte block at byte ((t * KT) + kt) * 18432 with
+ *     KT = ceil(K / 256).  Inside a block: bytes [0, 16384) hold the codes of
+ *     the 128 rows, row rr at rr * 128, its 16-byte chunk c (K elements
+ *     kt*256 + 32c .. +32) stored at chunk position c XOR (rr % 8) (the
+ *     128-byte swizzle); bytes [16384, 18432) hold the tile's scales as four
+ *     512-byte atoms (one per 64 K-elements) with the atom layout above.
+ *     Chunks and atoms past K (a partial last K tile) are never read.
+ *   Prepared rows: for the gate_up weights (N = 2I) the rows are interleaved
+ *     in blocks of 64: prepared row 128*b + j is gate row 64*b + j and
+ *     prepared row 128*b + 64 + j is up row 64*b + j (j < 64).  The down
+ *     weights keep their row order.
  */
 #ifndef NVFP4_MOE_H
 #define NVFP4_MOE_H
@@ -80,14 +90,14 @@ typedef enum {
   MOE_ERR_WORKSPACE = 7    /* workspace pointer null or smaller than the size query asks for */
 } moe_status;
 
-enum { MOE_SF_LINEAR = 0, MOE_SF_TILED = 1 };
+enum { MOE_SF_LINEAR = 0, MOE_SF_TILED = 1, MOE_SF_BLOCKED = 2 };
 enum { MOE_IN_BF16 = 0, MOE_IN_F32 = 1 };
 enum { MOE_EPI_NONE = 0, MOE_EPI_SILU_MUL_QUANT = 1, MOE_EPI_FINALIZE = 2 };
 
 /* Human-readable name of a status code (static string). */
 MOE_API const char* moe_status_string(int status);
 
-/* ABI version of this header; bumped on any incompatible change. */
+/* ABI version of this header; bumped on any incompatible change (2: blocked weights). */
 MOE_API int moe_abi_version(void);
 
 /* Reads and clears the device error word written by bounded waits that gave
@@ -104,6 +114,10 @@ MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
  * first pipeline stage, so the bounded-wait path can be exercised without
  * faulting anything.  0 (the default) for normal operation. */
 MOE_API void moe_debug_set_flags(int flags);
+
+/* Bytes of a blocked weight buffer of `rows` rows (rows % 128 == 0) and K
+ * columns (K % 64 == 0); 0 if the shape is not supported. */
+MOE_API size_t moe_blocked_weight_bytes(int64_t rows, int K);
 
 /* Upper bound, for the caller's allocation, of the padded routed rows of R
  * routed rows over E experts: R + 127 * min(E, R), rounded up to 128. */
@@ -153,10 +167,14 @@ MOE_API moe_status moe_route_permute(const float* logits, int T, int E, int k, i
  *   dst_row       i32 [n_items] or NULL: item i is written to output row
  *                 dst_row[i] (NULL: row i)
  *   codes         u8 [dst_rows_alloc][K/2]           out
+ *                 (MOE_SF_BLOCKED: the blocked weight buffer, codes and
+ *                 scales together, moe_blocked_weight_bytes(dst_rows_alloc, K))
  *   sf            u8, linear [dst_rows_alloc][K/16] or tiled over
- *                 dst_rows_alloc rows (sf_layout)   out
+ *                 dst_rows_alloc rows (sf_layout); unused (may be NULL) for
+ *                 MOE_SF_BLOCKED                     out
  *   ws / ws_bytes workspace of nvfp4_quantize_workspace_size(groups) bytes
- * Requires K % 16 == 0 (K % 64 == 0 and dst_rows_alloc % 128 == 0 for tiled),
+ * Requires K % 16 == 0 (K % 64 == 0 and dst_rows_alloc % 128 == 0 for tiled
+ * and blocked),
  * src_rows % groups == 0.  Rows of the output not named by any item are left
  * untouched.  Deterministic, bit-exact with the definition above.
  * ------------------------------------------------------------------------- */
@@ -190,12 +208,15 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  * Arguments:
  *   a_codes/a_sf  activations, padded-row layout, tiled scales, a_rows_alloc rows
  *   a_scale       f32 [1] decode multiplier of A
- *   b_codes/b_sf  prepared expert weights [E][N][K/2], tiled scales
+ *   b_blocked     prepared expert weights, blocked layout over E*N rows
  *   b_scale       f32 [E]
  *   expert_offsets i32 [E+1] (as moe_route_permute writes them)
  *   ep            host pointer to epilogue arguments (NULL for NONE)
  *   ws / ws_bytes workspace of moe_grouped_gemm_workspace_size(...) bytes
- * Requires K % 64 == 0, N % 128 == 0 (and N/2 % 64 == 0 for SILU_MUL_QUANT),
+ * Tiling: the kernel takes 128 weight rows per tile as the MMA M dimension and
+ * up to 64 (decode regime: the allocation implies <= 48 routed rows per
+ * expert on average) or 128 (otherwise) routed rows as MMA N.
+ * Requires K % 64 == 0, N % 128 == 0,
  * E <= 1024, a_rows_alloc % 128 == 0, all pointers 16-byte aligned.
  * ------------------------------------------------------------------------- */
 typedef struct {
@@ -214,7 +235,7 @@ typedef struct {
 
 MOE_API size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int N);
 MOE_API moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
-                                  const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,
+                                  const uint8_t* b_blocked, const float* b_scale,
                                   const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,
                                   int epilogue, const moe_epilogue_args* ep, void* out, void* ws, size_t ws_bytes,
                                   void* stream);
@@ -238,6 +259,16 @@ MOE_API moe_status moe_finalize(const uint16_t* y, const float* topk_w, const in
                         uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_fp4_mma_probe -- measurement aid: enqueues one launch that issues
+ * `iters` back-to-back dense NVFP4 MMAs (the grouped GEMM's instruction,
+ * M = 128, N = 256, K = 64, operands in shared memory, no global-memory
+ * traffic) on each of `blocks` CTAs (0 = one per SM).  The caller times the
+ * launch on `stream`; *flops_per_launch (host) receives the FLOPs it performs.
+ * Gives the dense FP4 tensor rate the prefill roofline is measured against.
+ * ------------------------------------------------------------------------- */
+MOE_API moe_status moe_fp4_mma_probe(int iters, int blocks, double* flops_per_launch, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_forward -- the fused MoE layer: route + permute, quantise x into the
  * routed rows, gate_up GEMM with SiLU-mul + requantise epilogue, down GEMM
  * with FINALIZE epilogue.  Same definitions as the calls above.
@@ -251,11 +282,9 @@ MOE_API moe_status moe_finalize(const uint16_t* y, const float* topk_w, const in
  * Requires H % 128 == 0, I % 64 == 0, plus the requirements above.
  * ------------------------------------------------------------------------- */
 typedef struct {
-  const uint8_t* w13_codes; /* [E][2I][H/2], gate/up interleaved */
-  const uint8_t* w13_sf;    /* tiled over E*2I rows */
+  const uint8_t* w13;       /* blocked, E*2I rows x H, gate/up interleaved */
   const float* w13_scale;   /* [E] */
-  const uint8_t* w2_codes;  /* [E][H][I/2] */
-  const uint8_t* w2_sf;     /* tiled over E*H rows */
+  const uint8_t* w2;        /* blocked, E*H rows x I */
   const float* w2_scale;    /* [E] */
 } moe_weights;
 

@@ -22,11 +22,12 @@ from . import _lib
 from ._lib import EpilogueArgs, ForwardLayout, MoeError, Weights
 
 EPI_NONE, EPI_SILU_MUL_QUANT, EPI_FINALIZE = 0, 1, 2
-SF_LINEAR, SF_TILED = 0, 1
+SF_LINEAR, SF_TILED, SF_BLOCKED = 0, 1, 2
 
 __all__ = ["moe_route_permute", "nvfp4_quantize", "moe_grouped_gemm_nvfp4", "moe_finalize", "moe_forward",
            "prepare_expert_weights", "MoeForward", "padded_rows_max", "device_error", "EPI_NONE",
-           "EPI_SILU_MUL_QUANT", "EPI_FINALIZE", "SF_LINEAR", "SF_TILED", "MoeError"]
+           "EPI_SILU_MUL_QUANT", "EPI_FINALIZE", "SF_LINEAR", "SF_TILED", "SF_BLOCKED", "MoeError",
+           "EpilogueArgs"]
 
 
 def _L():
@@ -74,6 +75,21 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def debug_set_flags(flags: int) -> None:
     _L().moe_debug_set_flags(int(flags))
+
+
+def fp4_mma_peak_tflops(iters: int = 20000, reps: int = 5) -> float:
+    """Dense NVFP4 MMA rate of this GPU (TFLOP/s), timed with CUDA events over `reps` probe launches."""
+    L = _L()
+    flops = ctypes.c_double(0.0)
+    s = torch.cuda.current_stream()
+    _check("moe_fp4_mma_probe", L.moe_fp4_mma_probe(1000, 0, ctypes.byref(flops), _stream(s)))  # warm-up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(reps):
+        _check("moe_fp4_mma_probe", L.moe_fp4_mma_probe(iters, 0, ctypes.byref(flops), _stream(s)))
+    b.record(s)
+    b.synchronize()
+    return flops.value * reps / (a.elapsed_time(b) / 1e3) / 1e12
 
 
 # ---------------------------------------------------------------- routing
@@ -130,12 +146,16 @@ def nvfp4_quantize(x: torch.Tensor, tensor_scale: torch.Tensor | None = None, gr
     dynamic = tensor_scale is None
     if dynamic:
         tensor_scale = _empty(groups, torch.float32, dev)
-    if codes is None:
-        codes = torch.zeros((dst_rows_alloc, K // 2), dtype=torch.uint8, device=dev)
-    if sf is None:
-        sf = torch.zeros((dst_rows_alloc * (K // 16),), dtype=torch.uint8, device=dev)
-        if sf_layout == SF_LINEAR:
-            sf = sf.view(dst_rows_alloc, K // 16)
+    if sf_layout == SF_BLOCKED:
+        if codes is None:
+            codes = torch.zeros(int(_L().moe_blocked_weight_bytes(dst_rows_alloc, K)), dtype=torch.uint8, device=dev)
+    else:
+        if codes is None:
+            codes = torch.zeros((dst_rows_alloc, K // 2), dtype=torch.uint8, device=dev)
+        if sf is None:
+            sf = torch.zeros((dst_rows_alloc * (K // 16),), dtype=torch.uint8, device=dev)
+            if sf_layout == SF_LINEAR:
+                sf = sf.view(dst_rows_alloc, K // 16)
     L = _L()
     wsb = L.nvfp4_quantize_workspace_size(groups)
     ws = _empty(max(wsb, 256), torch.uint8, dev)
@@ -147,9 +167,9 @@ def nvfp4_quantize(x: torch.Tensor, tensor_scale: torch.Tensor | None = None, gr
 
 @dataclass
 class PreparedWeights:
-    codes: torch.Tensor   # uint8 [E, N, K/2] (gate/up interleaved for gate_up)
-    sf: torch.Tensor      # uint8 tiled over E*N rows
-    scale: torch.Tensor   # float32 [E]
+    blocked: torch.Tensor  # uint8, blocked layout over E*N rows (gate/up interleaved for gate_up)
+    scale: torch.Tensor    # float32 [E]
+    E: int
     N: int
     K: int
 
@@ -171,9 +191,9 @@ def prepare_expert_weights(w: torch.Tensor, gate_up: bool, stream=None) -> Prepa
     if gate_up:
         local = gate_up_row_map(N, dev).to(torch.int64)
         dst = (torch.arange(E, device=dev, dtype=torch.int64)[:, None] * N + local[None, :]).reshape(-1).to(torch.int32)
-    codes, sf, scale = nvfp4_quantize(w.reshape(E * N, K), None, groups=E, dst_row=dst, sf_layout=SF_TILED,
-                                      dst_rows_alloc=E * N, stream=stream)
-    return PreparedWeights(codes.view(E, N, K // 2), sf, scale, N, K)
+    blocked, _, scale = nvfp4_quantize(w.reshape(E * N, K), None, groups=E, dst_row=dst, sf_layout=SF_BLOCKED,
+                                       dst_rows_alloc=E * N, stream=stream)
+    return PreparedWeights(blocked, scale, E, N, K)
 
 
 # ---------------------------------------------------------------- grouped GEMM
@@ -183,7 +203,7 @@ def moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, w: PreparedWeights, expert_of
                            perm_to_expanded=None, topk_w=None, T: int = 0, k: int = 0, out=None, stream=None):
     """Expert-grouped NVFP4 GEMM over routed rows (padded-row layout, tiled scales)."""
     rows_alloc = a_codes.shape[0]
-    E = w.codes.shape[0]
+    E = w.E
     dev = a_codes.device
     ep = EpilogueArgs()
     wsb = 0
@@ -212,7 +232,7 @@ def moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, w: PreparedWeights, expert_of
         wsb = _L().moe_grouped_gemm_workspace_size(epilogue, T, w.N)
         ws = _empty(wsb, torch.uint8, dev)
     _check("moe_grouped_gemm_nvfp4", _L().moe_grouped_gemm_nvfp4(
-        _ptr(a_codes), _ptr(a_sf), _ptr(a_scale), _ptr(w.codes), _ptr(w.sf), _ptr(w.scale), _ptr(expert_offsets), E,
+        _ptr(a_codes), _ptr(a_sf), _ptr(a_scale), _ptr(w.blocked), _ptr(w.scale), _ptr(expert_offsets), E,
         rows_alloc, w.N, w.K, epilogue, ctypes.byref(ep), _ptr(out) if out is not None else None, _ptr(ws), wsb,
         _stream(stream)))
     if epilogue == EPI_SILU_MUL_QUANT:
@@ -253,7 +273,7 @@ class MoeForward:
     def __call__(self, x, logits, w13: PreparedWeights, w2: PreparedWeights, h_scale: float, out=None, stream=None):
         if out is None:
             out = _empty((self.T, self.H), torch.bfloat16, x.device)
-        wts = Weights(_ptr(w13.codes), _ptr(w13.sf), _ptr(w13.scale), _ptr(w2.codes), _ptr(w2.sf), _ptr(w2.scale))
+        wts = Weights(_ptr(w13.blocked), _ptr(w13.scale), _ptr(w2.blocked), _ptr(w2.scale))
         _check("moe_forward", _L().moe_forward(
             _ptr(x), _ptr(logits), ctypes.byref(wts), self.T, self.E, self.k, self.H, self.I, float(h_scale),
             _ptr(out), _ptr(self.ws), self.layout.total, _stream(stream)))

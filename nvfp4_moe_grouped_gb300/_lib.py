@@ -32,11 +32,9 @@ class EpilogueArgs(ctypes.Structure):
 class Weights(ctypes.Structure):
     """Mirror of moe_weights."""
     _fields_ = [
-        ("w13_codes", c_void_p),
-        ("w13_sf", c_void_p),
+        ("w13", c_void_p),
         ("w13_scale", c_void_p),
-        ("w2_codes", c_void_p),
-        ("w2_sf", c_void_p),
+        ("w2", c_void_p),
         ("w2_scale", c_void_p),
     ]
 
@@ -57,15 +55,17 @@ SIGNATURES = {
     "moe_set_wait_timeout_ns": (None, [c_uint64]),
     "moe_debug_set_flags": (None, [c_int]),
     "moe_padded_rows_max": (c_int64, [c_int64, c_int]),
+    "moe_blocked_weight_bytes": (c_size_t, [c_int64, c_int]),
     "moe_route_permute_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_route_permute": (c_int, [c_void_p, c_int, c_int, c_int] + [c_void_p] * 7 + [c_size_t, c_void_p]),
     "nvfp4_quantize_workspace_size": (c_size_t, [c_int]),
     "nvfp4_quantize": (c_int, [c_void_p, c_int, c_int64, c_int, c_int, c_void_p, c_int, c_int64, c_int, c_void_p,
                                c_void_p, c_void_p, c_int, c_int64, c_void_p, c_size_t, c_void_p]),
     "moe_grouped_gemm_workspace_size": (c_size_t, [c_int, c_int, c_int]),
-    "moe_grouped_gemm_nvfp4": (c_int, [c_void_p] * 7 + [c_int, c_int64, c_int, c_int, c_int, c_void_p, c_void_p,
+    "moe_grouped_gemm_nvfp4": (c_int, [c_void_p] * 6 + [c_int, c_int64, c_int, c_int, c_int, c_void_p, c_void_p,
                                                         c_void_p, c_size_t, c_void_p]),
     "moe_finalize": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "moe_fp4_mma_probe": (c_int, [c_int, c_int, c_void_p, c_void_p]),
     "moe_forward_workspace_size": (c_size_t, [c_int] * 5),
     "moe_forward_workspace_layout": (c_int, [c_int] * 5 + [c_void_p]),
     "moe_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,

@@ -27,6 +27,11 @@ moe_status check_launch();              // maps cudaGetLastError to a status
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Blocked weight layout: one block per 128 rows x 256 K-elements, holding the
+// 128-byte-swizzled code tile (16 KB, the shared-memory image the MMA reads)
+// followed by its four 512-byte scale atoms.
+constexpr int kBlockedTileBytes = 16384 + 2048;
+
 // ----------------------------------------------------------------------------
 // Scalars
 // ----------------------------------------------------------------------------

@@ -54,8 +54,7 @@ extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const 
                                   int H, int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes,
                                   void* stream) {
   if (!x || !logits || !w || !out) return MOE_ERR_INVALID_ARG;
-  if (!w->w13_codes || !w->w13_sf || !w->w13_scale || !w->w2_codes || !w->w2_sf || !w->w2_scale)
-    return MOE_ERR_INVALID_ARG;
+  if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale) return MOE_ERR_INVALID_ARG;
   if (T < 1 || E < 1 || k < 1 || k > E || H < 1 || I < 1 || !(h_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
   if (H % 128 || I % 64) return MOE_ERR_UNSUPPORTED;
   moe_forward_layout L;
@@ -90,7 +89,7 @@ extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const 
   ep.h_scale_out = hs;
   ep.h_codes = h_codes;
   ep.h_sf = h_sf;
-  s = moe_grouped_gemm_nvfp4(x_codes, x_sf, x_scale, w->w13_codes, w->w13_sf, w->w13_scale, offs, E, L.padded_rows,
+  s = moe_grouped_gemm_nvfp4(x_codes, x_sf, x_scale, w->w13, w->w13_scale, offs, E, L.padded_rows,
                              2 * I, H, MOE_EPI_SILU_MUL_QUANT, &ep, nullptr, nullptr, 0, stream);
   if (s != MOE_OK) return s;
   moe_epilogue_args ep2{};
@@ -98,7 +97,7 @@ extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const 
   ep2.topk_w = topk_w;
   ep2.T = T;
   ep2.k = k;
-  return moe_grouped_gemm_nvfp4(h_codes, h_sf, hs, w->w2_codes, w->w2_sf, w->w2_scale, offs, E, L.padded_rows, H, I,
+  return moe_grouped_gemm_nvfp4(h_codes, h_sf, hs, w->w2, w->w2_scale, offs, E, L.padded_rows, H, I,
                                 MOE_EPI_FINALIZE, &ep2, out, at(L.gemm_ws),
                                 moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, H), stream);
 }

@@ -14,20 +14,29 @@
 // Design (GB300, one CTA per SM, persistent):
 //   * Operand roles are swapped relative to the row-major problem: the 128
 //     weight rows of a tile are the MMA M dimension and the expert's routed
-//     token rows (up to 128) are MMA N.  At decode an expert sees 4-64 rows,
-//     so every weight tile is streamed from HBM exactly once per 128 routed
-//     rows and the tensor core never waits on padding.
-//   * Work unit = (expert, 128-row block of its routed rows, 128-row weight
-//     tile), full K.  Units are ordered expert-major so the ~150 CTAs running
+//     rows (up to BN) are MMA N.  At decode an expert sees 4-64 rows, so every
+//     weight tile is streamed from HBM once per BN routed rows and the tensor
+//     core never computes padding rows of M.
+//   * The routed-row tile BN is picked per launch from the rows-per-expert
+//     regime: BN = 64 with 7 pipeline stages for decode, BN = 128 with 5
+//     stages when experts see more rows (prefill).
+//   * Work unit = (expert, BN-row block of its routed rows, 128-row weight
+//     tile), full K.  Units are ordered expert-major so the CTAs running
 //     together share each expert's token tile in L2.  CTA c takes units c,
 //     c + grid, ...
-//   * Warp roles: warp 0 issues TMA (weights and tokens: 2D tensor maps with
-//     128-byte swizzle; scales: 1D bulk copies of the tiled 512-byte atoms),
-//     warp 1 owns tensor memory and issues tcgen05.cp (scales -> TMEM) and
-//     tcgen05.mma, warps 2-5 drain the accumulator (tcgen05.ld) and run the
-//     epilogue.  A 5-stage shared-memory ring (36 KB per stage) keeps ~180 KB
-//     of loads in flight per SM; two TMEM accumulators let the epilogue of
-//     one unit overlap the mainloop of the next.
+//   * Weights are prepared in a blocked layout: per 128 rows x 256 K-elements
+//     one contiguous 18 KB block holding the 128-byte-swizzled code tile (the
+//     exact shared-memory image the MMA descriptor reads) and its four scale
+//     atoms, so each pipeline stage of weights is ONE linear bulk copy that
+//     streams a contiguous 18 KB run of HBM.
+//   * Warp roles: warp 0 issues the copies (weights: bulk copy, evict-first;
+//     routed rows: 2D tensor-map loads of 32 rows with 128-byte swizzle and
+//     a bulk copy of their scale atoms, evict-last), warp 1 owns tensor memory
+//     and issues tcgen05.cp (scales -> TMEM) and tcgen05.mma, warps 2-5 drain
+//     the accumulator (tcgen05.ld) and run the epilogue.  Two TMEM
+//     accumulators let the epilogue of one unit overlap the mainloop of the
+//     next; every stage has its own TMEM scale slot, recycled by the same
+//     commit that frees the stage.
 //   * Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT in the
 //     device error word, lets its own copies and MMAs finish, frees its tensor
 //     memory and returns.
@@ -38,39 +47,40 @@ moe_status launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStr
 
 namespace {
 
-constexpr int kBM = 128;                       // weight rows per tile (MMA M)
-constexpr int kBK = 256;                       // K elements per stage (128 bytes per row)
-constexpr int kBNMax = 128;                    // routed rows per tile (MMA N <= 128)
-constexpr int kStages = 5;
-constexpr int kWStageBytes = kBM * kBK / 2;    // 16 KB
-constexpr int kXStageBytes = kBNMax * kBK / 2; // 16 KB
-constexpr int kSfStageBytes = 4 * 512;         // 4 scale atoms (one per 64-element K step)
+constexpr int kBM = 128;                  // weight rows per tile (MMA M)
+constexpr int kBK = 256;                  // K elements per stage (128 bytes per row)
+constexpr int kWStageBytes = kBlockedTileBytes;  // 16 KB codes + 2 KB scale atoms
+constexpr int kSfStageBytes = 4 * 512;    // scale atoms of the routed rows (one per 64-element K step)
 constexpr int kThreads = 192;
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = kBNMax;          // per accumulator buffer
-constexpr uint32_t kSfTmemBase = 2 * kAccCols; // scale slots after the two accumulators
-constexpr uint32_t kSfSlotCols = 32;           // 16 columns weight scales + 16 columns token scales
-static_assert(kSfTmemBase + kStages * kSfSlotCols <= kTmemCols, "tensor memory budget");
+constexpr uint32_t kSfSlotCols = 32;      // 16 columns weight scales + 16 columns routed-row scales
 
-struct SmemLayout {
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 64 ? 7 : 5;
+  static constexpr int kXStageBytes = BN * kBK / 2;
+  static constexpr uint32_t kAccCols = BN;
+  static constexpr uint32_t kSfTmemBase = 2 * BN;
+  static_assert(kSfTmemBase + kStages * kSfSlotCols <= kTmemCols, "tensor memory budget");
+  // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int w = 0;
   static constexpr int x = w + kStages * kWStageBytes;
-  static constexpr int sfw = x + kStages * kXStageBytes;
-  static constexpr int sfx = sfw + kStages * kSfStageBytes;
-  static constexpr int epi = sfx + kStages * kSfStageBytes;            // float [32][65]
-  static constexpr int tok_t = epi + 32 * 65 * 4;                       // int [128]
-  static constexpr int tok_w = tok_t + kBNMax * 4;                      // float [128]
-  static constexpr int bars = tok_w + kBNMax * 4;                       // uint64 [2*kStages + 5]
-  static constexpr int misc = bars + (2 * kStages + 5) * 8;             // tmem base, abort
-  static constexpr int sched = misc + 16;                               // int [3][kMaxExperts+1]
+  static constexpr int sfx = x + kStages * kXStageBytes;
+  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][65]
+  static constexpr int tok_t = epi + 32 * 65 * 4;            // int [BN]
+  static constexpr int tok_w = tok_t + BN * 4;               // float [BN]
+  static constexpr int bars = tok_w + BN * 4;                // uint64 [2*kStages + 5]
+  static constexpr int misc = bars + (2 * kStages + 5) * 8;  // tmem base, abort flag
+  static constexpr int sched = misc + 16;                    // int [3][kMaxExperts+1]
   static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
+  static constexpr int smem_bytes = total + 1024;            // + alignment slack
+  static_assert(smem_bytes <= 232448, "shared memory budget");
+  static_assert(x % 1024 == 0 && kXStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
-constexpr int kSmemBytes = SmemLayout::total + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct GemmParams {
-  const uint8_t* w_sf;        // tiled scales of the weights (E*N rows)
+  const uint8_t* w_blocked;   // prepared weights, blocked layout over E*N rows
   const uint8_t* x_sf;        // tiled scales of the routed rows
   const float* x_scale;       // [1]
   const float* w_scale;       // [E]
@@ -94,7 +104,7 @@ struct GemmParams {
 };
 
 struct Unit {
-  int e, nb, mt, rows, n_mma, x_row, w_row, m_off;
+  int e, nb, mt, rows, n_mma, x_row, m_off;
   bool valid;  // false when the offsets place the unit outside the routed-row allocation
 };
 
@@ -107,20 +117,21 @@ MOE_DEVINL int find_expert(const int* start, int E, int u) {
   return lo;
 }
 
+template <int BN>
 MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MT,
                             int64_t rows_alloc) {
   Unit d;
   d.e = find_expert(unit_start, E, u);
-  int local = u - unit_start[d.e];
+  const int local = u - unit_start[d.e];
   d.nb = local / MT;
   d.mt = local - d.nb * MT;
-  int m_e = off[d.e + 1] - off[d.e];
-  d.rows = min(kBNMax, m_e - d.nb * kBNMax);
+  const int m_e = off[d.e + 1] - off[d.e];
+  d.rows = min(BN, m_e - d.nb * BN);
   d.n_mma = d.rows <= 32 ? 32 : (d.rows <= 64 ? 64 : 128);
-  d.x_row = pad_start[d.e] + d.nb * kBNMax;
-  d.m_off = off[d.e] + d.nb * kBNMax;
-  d.w_row = 0;  // set by caller (needs N)
-  d.valid = d.rows > 0 && static_cast<int64_t>(d.x_row) + kBNMax <= rows_alloc;
+  if (d.n_mma > BN) d.n_mma = BN;
+  d.x_row = pad_start[d.e] + d.nb * BN;
+  d.m_off = off[d.e] + d.nb * BN;
+  d.valid = d.rows > 0 && static_cast<int64_t>(d.x_row) + BN <= rows_alloc;
   return d;
 }
 
@@ -141,26 +152,27 @@ MOE_DEVINL bool epi_any(bool pred) {
   return r != 0;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                        const GemmParams p) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const GemmParams p) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_w = smem + SmemLayout::w;
-  uint8_t* s_x = smem + SmemLayout::x;
-  uint8_t* s_sfw = smem + SmemLayout::sfw;
-  uint8_t* s_sfx = smem + SmemLayout::sfx;
-  float* s_epi = reinterpret_cast<float*>(smem + SmemLayout::epi);
-  int* s_tok_t = reinterpret_cast<int*>(smem + SmemLayout::tok_t);
-  float* s_tok_w = reinterpret_cast<float*>(smem + SmemLayout::tok_w);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars);
-  uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
+  uint8_t* s_w = smem + C::w;
+  uint8_t* s_x = smem + C::x;
+  uint8_t* s_sfx = smem + C::sfx;
+  float* s_epi = reinterpret_cast<float*>(smem + C::epi);
+  int* s_tok_t = reinterpret_cast<int*>(smem + C::tok_t);
+  float* s_tok_w = reinterpret_cast<float*>(smem + C::tok_w);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bars);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SmemLayout::misc + 4);
-  int* unit_start = reinterpret_cast<int*>(smem + SmemLayout::sched);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::misc + 4);
+  int* unit_start = reinterpret_cast<int*>(smem + C::sched);
   int* pad_start = unit_start + (kMaxExperts + 1);
   int* off = pad_start + (kMaxExperts + 1);
 
@@ -171,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- prologue: barriers, tensor memory, work list --------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -182,31 +194,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == 0) {
-    // unit_start[e]: first unit of expert e; pad_start[e]: first padded row.
+    // unit_start[e]: first unit of expert e; pad_start[e]: first padded row (128-row padding).
     const int per = (E + 31) / 32;
     const int e0 = lane * per;
     int units = 0, pads = 0;
     for (int e = e0; e < min(E, e0 + per); ++e) {
-      int m = __ldg(p.expert_offsets + e + 1) - __ldg(p.expert_offsets + e);
-      int blocks = (m + kBNMax - 1) / kBNMax;
-      units += blocks * MT;
-      pads += blocks * kBNMax;
+      const int m = __ldg(p.expert_offsets + e + 1) - __ldg(p.expert_offsets + e);
+      units += ((m + BN - 1) / BN) * MT;
+      pads += ((m + 127) / 128) * 128;
     }
     int iu = units, ip = pads;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int yu = __shfl_up_sync(0xffffffffu, iu, o), yp = __shfl_up_sync(0xffffffffu, ip, o);
+      const int yu = __shfl_up_sync(0xffffffffu, iu, o), yp = __shfl_up_sync(0xffffffffu, ip, o);
       if (lane >= o) { iu += yu; ip += yp; }
     }
     int ru = iu - units, rp = ip - pads;
     for (int e = e0; e < min(E, e0 + per); ++e) {
-      int o0 = __ldg(p.expert_offsets + e), o1 = __ldg(p.expert_offsets + e + 1);
+      const int o0 = __ldg(p.expert_offsets + e), o1 = __ldg(p.expert_offsets + e + 1);
       unit_start[e] = ru;
       pad_start[e] = rp;
       off[e] = o0;
-      int blocks = (o1 - o0 + kBNMax - 1) / kBNMax;
-      ru += blocks * MT;
-      rp += blocks * kBNMax;
+      ru += ((o1 - o0 + BN - 1) / BN) * MT;
+      rp += ((o1 - o0 + 127) / 128) * 128;
     }
     if (lane == 31) {
       unit_start[E] = iu;
@@ -221,21 +231,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_units = unit_start[E];
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- producer ----------------
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      int issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      int issued[S];
+      for (int s = 0; s < S; ++s) issued[s] = 0;
       bool skip_once = (p.debug_flags & 1) != 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        Unit d = decode_unit(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
         if (!d.valid) continue;
-        const int w_row = d.e * N + d.mt * kBM;
-        const uint8_t* sfw_src = p.w_sf + static_cast<int64_t>(w_row / 128) * (K / 64) * 512;
+        const uint8_t* w_src = p.w_blocked + static_cast<int64_t>(d.e * MT + d.mt) * KT * kWStageBytes;
         const uint8_t* sfx_src = p.x_sf + static_cast<int64_t>(d.x_row / 128) * (K / 64) * 512;
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, s_abort)) {
@@ -248,22 +257,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (skip_once) {
             skip_once = false;  // test hook: this stage is never filled
           } else {
-            const uint32_t bytes = kWStageBytes + d.n_mma * (kBK / 2) + 2 * steps * 512;
+            const uint32_t bytes = kWStageBytes + d.n_mma * (kBK / 2) + steps * 512;
             mbar_arrive_expect_tx(&full[stage], bytes);
-            tma_load_2d(s_w + stage * kWStageBytes, &tm_w, &full[stage], kt * (kBK / 2), w_row, pol_w);
+            bulk_load(s_w + stage * kWStageBytes, w_src + static_cast<int64_t>(kt) * kWStageBytes, kWStageBytes,
+                      &full[stage], pol_w);
             for (int q = 0; q < d.n_mma / 32; ++q)
-              tma_load_2d(s_x + stage * kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage], kt * (kBK / 2),
+              tma_load_2d(s_x + stage * C::kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage], kt * (kBK / 2),
                           d.x_row + 32 * q, pol_x);
-            bulk_load(s_sfw + stage * kSfStageBytes, sfw_src + kt * 4 * 512, steps * 512, &full[stage], pol_w);
             bulk_load(s_sfx + stage * kSfStageBytes, sfx_src + kt * 4 * 512, steps * 512, &full[stage], pol_x);
             issued[stage] += 1;
           }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
       // Let every copy this CTA started land before the CTA can exit.
       int zero = 0;
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < S; ++s)
         if (issued[s] > 0)
           mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.timeout_ns,
                             reinterpret_cast<volatile int*>(&zero));
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc_i = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++acc_i) {
-        Unit d = decode_unit(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
         if (!d.valid) { --acc_i; continue; }
         const int b = acc_i & 1;
         if (!mbar_wait_bounded(&acc_empty[b], ((acc_i >> 1) & 1) ^ 1u, p.timeout_ns, s_abort)) {
@@ -285,8 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * kAccCols;
+        const uint32_t d_tmem = tmem_base + b * C::kAccCols;
         const uint32_t idesc = idesc_mxf4nvf4(d.n_mma);
+        // The routed rows' scale atoms cover a 128-row block; this unit's rows start
+        // (x_row % 128) / 32 TMEM columns into each atom's four columns.
+        const uint32_t sfx_col_off = static_cast<uint32_t>((d.x_row & 127) >> 5);
         for (int kt = 0; kt < KT; ++kt) {
           if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 3);
@@ -296,22 +308,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const int steps = min(4, (K - kt * kBK) / 64);
-          const uint32_t sf_col = tmem_base + kSfTmemBase + stage * kSfSlotCols;
-          const uint32_t sfw_addr = smem_u32(s_sfw + stage * kSfStageBytes);
+          const uint32_t sf_col = tmem_base + C::kSfTmemBase + stage * kSfSlotCols;
+          const uint32_t w_addr = smem_u32(s_w + stage * kWStageBytes);
+          const uint32_t sfw_addr = w_addr + 16384;
           const uint32_t sfx_addr = smem_u32(s_sfx + stage * kSfStageBytes);
           for (int g = 0; g < steps; ++g) {
             tmem_cp_32x128b_x4(sf_col + 4 * g, smem_desc(sfw_addr + 512 * g, 0, 128, 0));
             tmem_cp_32x128b_x4(sf_col + 16 + 4 * g, smem_desc(sfx_addr + 512 * g, 0, 128, 0));
           }
-          const uint32_t w_addr = smem_u32(s_w + stage * kWStageBytes);
-          const uint32_t x_addr = smem_u32(s_x + stage * kXStageBytes);
+          const uint32_t x_addr = smem_u32(s_x + stage * C::kXStageBytes);
           for (int g = 0; g < steps; ++g) {
             const uint64_t adesc = smem_desc(w_addr + 32 * g, 16, 1024, 2);
             const uint64_t bdesc = smem_desc(x_addr + 32 * g, 16, 1024, 2);
-            mma_mxf4nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * g, sf_col + 16 + 4 * g, (kt | g) != 0);
+            mma_mxf4nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * g, sf_col + 16 + 4 * g + sfx_col_off,
+                         (kt | g) != 0);
           }
           mma_commit(&empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         mma_commit(&acc_full[b]);
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && et == 0) *p.h_scale_out = p.h_scale;
     int acc_i = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
-      Unit d = decode_unit(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
       if (!d.valid) {
         if (et == 0) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
         --acc_i;
@@ -349,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const float alpha = x_scale * __ldg(p.w_scale + d.e);
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kAccCols;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAccCols;
       if (p.epilogue == MOE_EPI_FINALIZE) {
         if (et < d.rows) {
           const int ex = __ldg(p.perm_to_expanded + d.m_off + et);
@@ -466,11 +479,33 @@ bool make_code_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int BN>
+moe_status launch_gemm(const CUtensorMap& tm_x, const GemmParams& p, int64_t max_units, cudaStream_t st) {
+  using C = Cfg<BN>;
+  if (cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes) !=
+      cudaSuccess)
+    return MOE_ERR_RESOURCE;
+  int grid = num_sms();
+  if (grid < 1) return MOE_ERR_CUDA;
+  if (max_units < grid) grid = static_cast<int>(max_units);
+  grouped_gemm_kernel<BN><<<grid, kThreads, C::smem_bytes, st>>>(tm_x, p);
+  return check_launch();
+}
+
 }  // namespace
 
 int& gemm_debug_flags() {
   static int flags = 0;
   return flags;
+}
+
+// Routed-row tile of a launch from the rows-per-expert regime: the average
+// rows per expert the allocation implies (a_rows_alloc exceeds the routed rows
+// by at most 127 per expert).
+int gemm_tile_rows(int64_t a_rows_alloc, int E) {
+  const int64_t excess = 127ll * E;
+  const int64_t avg = a_rows_alloc > excess ? (a_rows_alloc - excess) / E : 0;
+  return avg <= 48 ? 64 : 128;
 }
 
 }  // namespace moe
@@ -485,19 +520,19 @@ extern "C" size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int N) {
 }
 
 extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
-                                             const uint8_t* b_codes, const uint8_t* b_sf, const float* b_scale,
+                                             const uint8_t* b_blocked, const float* b_scale,
                                              const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,
                                              int epilogue, const moe_epilogue_args* ep, void* out, void* ws,
                                              size_t ws_bytes, void* stream) {
-  if (!a_codes || !a_sf || !a_scale || !b_codes || !b_sf || !b_scale || !expert_offsets) return MOE_ERR_INVALID_ARG;
+  if (!a_codes || !a_sf || !a_scale || !b_blocked || !b_scale || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (E < 1 || a_rows_alloc < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_SILU_MUL_QUANT && epilogue != MOE_EPI_FINALIZE)
     return MOE_ERR_INVALID_ARG;
   if (E > kMaxExperts || K % 64 || N % kBM || a_rows_alloc % 128) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(E) * N > 0x7FFFFFFF || a_rows_alloc > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
-  if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(b_codes) || !aligned16(b_sf)) return MOE_ERR_MISALIGNED;
+  if (!aligned16(a_codes) || !aligned16(a_sf) || !aligned16(b_blocked)) return MOE_ERR_MISALIGNED;
   GemmParams p{};
-  p.w_sf = b_sf;
+  p.w_blocked = b_blocked;
   p.x_sf = a_sf;
   p.x_scale = a_scale;
   p.w_scale = b_scale;
@@ -512,7 +547,6 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
     p.out = out;
   } else if (epilogue == MOE_EPI_SILU_MUL_QUANT) {
     if (!ep || !ep->h_codes || !ep->h_sf) return MOE_ERR_INVALID_ARG;
-    if ((N / 2) % 64) return MOE_ERR_UNSUPPORTED;
     if (!(ep->h_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(ep->h_codes) || !aligned16(ep->h_sf)) return MOE_ERR_MISALIGNED;
     p.h_scale = ep->h_scale;
@@ -537,24 +571,16 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   p.debug_flags = gemm_debug_flags();
   if (!p.err) return MOE_ERR_CUDA;
 
-  CUtensorMap tm_w, tm_x;
-  if (!make_code_map(&tm_w, b_codes, static_cast<uint64_t>(E) * N, K / 2, kBM)) return MOE_ERR_CUDA;
+  CUtensorMap tm_x;
   if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
-    return MOE_ERR_RESOURCE;
-
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t max_units = (a_rows_alloc / kBNMax) * (N / kBM);
-  int grid = num_sms();
-  if (grid < 1) return MOE_ERR_CUDA;
-  if (max_units < grid) grid = static_cast<int>(max_units);
   if (epilogue == MOE_EPI_FINALIZE) {
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  grouped_gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(tm_w, tm_x, p);
-  moe_status s = check_launch();
+  const int bn = gemm_tile_rows(a_rows_alloc, E);
+  const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
+  moe_status s = bn == 64 ? launch_gemm<64>(tm_x, p, max_units, st) : launch_gemm<128>(tm_x, p, max_units, st);
   if (s != MOE_OK) return s;
   if (epilogue == MOE_EPI_FINALIZE)
     return launch_f32_to_bf16(static_cast<const float*>(ws), static_cast<uint16_t*>(out),

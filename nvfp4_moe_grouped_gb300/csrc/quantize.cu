@@ -71,7 +71,27 @@ __global__ void scale_from_amax_kernel(const uint32_t* __restrict__ amax_bits, i
   scale[g] = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
 }
 
-template <int IN_F32, int TILED>
+// Destination of one 16-element block (8 code bytes + 1 scale byte) of row `dst`, column block `c`.
+//   LAYOUT 0: linear codes and scales; 1: linear codes, tiled scales; 2: blocked weights (one
+//   18432-byte block per 128 rows x 256 K-elements: the 128-byte-swizzled code tile, then its
+//   four 512-byte scale atoms).
+template <int LAYOUT>
+MOE_DEVINL void block_dst(uint8_t* codes, uint8_t* sf, int64_t dst, int c, int K, uint8_t** code_at,
+                          uint8_t** sf_at) {
+  if (LAYOUT == 2) {
+    const int kt_count = (K + 255) / 256;
+    const int rr = static_cast<int>(dst & 127);
+    const int cc = c & 15;
+    uint8_t* base = codes + ((dst >> 7) * kt_count + (c >> 4)) * static_cast<int64_t>(kBlockedTileBytes);
+    *code_at = base + rr * 128 + (((cc >> 1) ^ (rr & 7)) << 4) + (cc & 1) * 8;
+    *sf_at = base + 16384 + (cc >> 2) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (cc & 3);
+  } else {
+    *code_at = codes + dst * (K / 2) + 8 * c;
+    *sf_at = (LAYOUT == 1) ? sf + tiled_sf_offset(dst, c, K) : sf + dst * (K / 16) + c;
+  }
+}
+
+template <int IN_F32, int LAYOUT>
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
     const void* __restrict__ x, int64_t rows_per_group, int K, const float* __restrict__ scale, int64_t n_items,
     int src_div, const int32_t* __restrict__ dst_row, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
@@ -95,11 +115,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
     for (int i = 0; i < 8; ++i) lo |= nvfp4_code(v[i], recip) << (4 * i);
 #pragma unroll
     for (int i = 0; i < 8; ++i) hi |= nvfp4_code(v[8 + i], recip) << (4 * i);
-    *reinterpret_cast<uint2*>(codes + dst * (K / 2) + 8 * c) = make_uint2(lo, hi);
-    if (TILED)
-      sf[tiled_sf_offset(dst, c, K)] = static_cast<uint8_t>(sfb);
-    else
-      sf[dst * nblk + c] = static_cast<uint8_t>(sfb);
+    uint8_t *code_at, *sf_at;
+    block_dst<LAYOUT>(codes, sf, dst, c, K, &code_at, &sf_at);
+    *reinterpret_cast<uint2*>(code_at) = make_uint2(lo, hi);
+    *sf_at = static_cast<uint8_t>(sfb);
   }
 }
 
@@ -107,6 +126,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
 }  // namespace moe
 
 using namespace moe;
+
+extern "C" size_t moe_blocked_weight_bytes(int64_t rows, int K) {
+  if (rows < 1 || K < 64 || rows % 128 || K % 64) return 0;
+  return static_cast<size_t>(rows / 128) * ((K + 255) / 256) * kBlockedTileBytes;
+}
 
 extern "C" size_t nvfp4_quantize_workspace_size(int groups) {
   if (groups < 1) return 0;
@@ -117,17 +141,18 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
                                      float* tensor_scale, int dynamic_scale, int64_t n_items, int src_div,
                                      const int32_t* dst_row, uint8_t* codes, uint8_t* sf, int sf_layout,
                                      int64_t dst_rows_alloc, void* ws, size_t ws_bytes, void* stream) {
-  if (!x || !tensor_scale || !codes || !sf) return MOE_ERR_INVALID_ARG;
+  if (!x || !tensor_scale || !codes || (!sf && sf_layout != MOE_SF_BLOCKED)) return MOE_ERR_INVALID_ARG;
   if (src_rows < 1 || K < 16 || groups < 1 || n_items < 0 || src_div < 1 || dst_rows_alloc < 1)
     return MOE_ERR_INVALID_ARG;
   if (in_dtype != MOE_IN_BF16 && in_dtype != MOE_IN_F32) return MOE_ERR_INVALID_ARG;
-  if (sf_layout != MOE_SF_LINEAR && sf_layout != MOE_SF_TILED) return MOE_ERR_INVALID_ARG;
+  if (sf_layout != MOE_SF_LINEAR && sf_layout != MOE_SF_TILED && sf_layout != MOE_SF_BLOCKED)
+    return MOE_ERR_INVALID_ARG;
   if (K % 16) return MOE_ERR_UNSUPPORTED;
-  if (sf_layout == MOE_SF_TILED && (K % 64 || dst_rows_alloc % 128)) return MOE_ERR_UNSUPPORTED;
+  if (sf_layout != MOE_SF_LINEAR && (K % 64 || dst_rows_alloc % 128)) return MOE_ERR_UNSUPPORTED;
   if (src_rows % groups) return MOE_ERR_INVALID_ARG;
   if ((n_items - 1) / src_div >= src_rows && n_items > 0) return MOE_ERR_INVALID_ARG;
   if (!dst_row && n_items > dst_rows_alloc) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(codes) || !aligned16(sf)) return MOE_ERR_MISALIGNED;
+  if (!aligned16(x) || !aligned16(codes) || (sf && !aligned16(sf))) return MOE_ERR_MISALIGNED;
   if (dynamic_scale && (!ws || ws_bytes < nvfp4_quantize_workspace_size(groups))) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t rows_per_group = src_rows / groups;
@@ -148,14 +173,19 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
   if (n_items > 0) {
     int64_t blocks = (n_items + kQuantWarps - 1) / kQuantWarps;
     if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
-    const bool f32 = in_dtype == MOE_IN_F32, tiled = sf_layout == MOE_SF_TILED;
+    const bool f32 = in_dtype == MOE_IN_F32;
 #define MOE_QLAUNCH(F, T)                                                                                     \
   quantize_kernel<F, T><<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, st>>>(                          \
       x, rows_per_group, K, tensor_scale, n_items, src_div, dst_row, codes, sf)
-    if (f32 && tiled) MOE_QLAUNCH(1, 1);
-    else if (f32) MOE_QLAUNCH(1, 0);
-    else if (tiled) MOE_QLAUNCH(0, 1);
-    else MOE_QLAUNCH(0, 0);
+    if (f32) {
+      if (sf_layout == MOE_SF_BLOCKED) MOE_QLAUNCH(1, 2);
+      else if (sf_layout == MOE_SF_TILED) MOE_QLAUNCH(1, 1);
+      else MOE_QLAUNCH(1, 0);
+    } else {
+      if (sf_layout == MOE_SF_BLOCKED) MOE_QLAUNCH(0, 2);
+      else if (sf_layout == MOE_SF_TILED) MOE_QLAUNCH(0, 1);
+      else MOE_QLAUNCH(0, 0);
+    }
 #undef MOE_QLAUNCH
   }
   return check_launch();

@@ -45,3 +45,32 @@ def padded_rows_of_items(expert_offsets: np.ndarray, topk_id_flat: np.ndarray, e
 
 def counts_to_offsets(counts) -> np.ndarray:
     return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def unblock_weights(blocked: torch.Tensor, rows: int, K: int):
+    """Linear codes [rows, K/2] and scales [rows, K/16] out of a blocked weight buffer.
+
+    Written from the blocked layout's definition: per 128 rows x 256 K-elements an
+    18432-byte block, codes row rr at rr*128 with 16-byte chunk c stored at chunk
+    c ^ (rr % 8), then four 512-byte scale atoms.
+    """
+    b = blocked.cpu().numpy().reshape(-1)
+    KT = (K + 255) // 256
+    codes = np.zeros((rows, K // 2), np.uint8)
+    sf = np.zeros((rows, K // 16), np.uint8)
+    r = np.arange(rows)
+    rr = r % 128
+    for kt in range(KT):
+        base = ((r // 128) * KT + kt) * 18432
+        for c in range(8):
+            if kt * 128 + 16 * c >= K // 2:
+                break
+            src = base + rr * 128 + ((c ^ (rr % 8)) * 16)
+            codes[:, kt * 128 + 16 * c:kt * 128 + 16 * c + 16] = b[src[:, None] + np.arange(16)[None, :]]
+        for cc in range(16):
+            col = kt * 16 + cc
+            if col >= K // 16:
+                break
+            src = base + 16384 + (cc // 4) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + cc % 4
+            sf[:, col] = b[src]
+    return codes, sf

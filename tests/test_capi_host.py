@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.moe_abi_version() == 1
+    assert L.moe_abi_version() == 2
     for s in range(8):
         assert L.moe_status_string(s)
     assert L.moe_status_string(99) == b"unknown status"
@@ -62,6 +62,13 @@ def test_forward_layout_is_consistent(L):
     assert lay.x_sf - lay.x_codes >= lay.padded_rows * 6144 // 2
     assert lay.total == L.moe_forward_workspace_size(1024, 256, 8, 6144, 2048)
     assert L.moe_forward_workspace_layout(4, 8, 9, 256, 128, ctypes.byref(lay)) == INVALID  # k > E
+
+
+def test_blocked_weight_bytes(L):
+    assert L.moe_blocked_weight_bytes(256 * 4096, 6144) == 256 * 32 * 24 * 18432
+    assert L.moe_blocked_weight_bytes(128, 320) == 2 * 18432      # partial last K tile takes a whole block
+    assert L.moe_blocked_weight_bytes(100, 256) == 0
+    assert L.moe_blocked_weight_bytes(128, 96) == 0
 
 
 def test_workspace_queries(L):
@@ -99,13 +106,13 @@ def test_quantize_rejects_before_launch(L):
 
 def test_grouped_gemm_rejects_before_launch(L):
     g = L.moe_grouped_gemm_nvfp4
-    base = [P] * 7
+    base = [P] * 6
     assert g(*base, 8, 128, 256, 288, moe.EPI_NONE, None, P, None, 0, None) == UNSUPPORTED      # K % 64
     assert g(*base, 8, 128, 200, 256, moe.EPI_NONE, None, P, None, 0, None) == UNSUPPORTED      # N % 128
     assert g(*base, 8, 100, 256, 256, moe.EPI_NONE, None, P, None, 0, None) == UNSUPPORTED      # rows % 128
     assert g(*base, 2048, 128, 256, 256, moe.EPI_NONE, None, P, None, 0, None) == UNSUPPORTED   # E
     assert g(*base, 8, 128, 256, 256, 9, None, P, None, 0, None) == INVALID                     # epilogue
-    assert g(Q, *[P] * 6, 8, 128, 256, 256, moe.EPI_NONE, None, P, None, 0, None) == MISALIGNED
+    assert g(Q, *[P] * 5, 8, 128, 256, 256, moe.EPI_NONE, None, P, None, 0, None) == MISALIGNED
     assert g(*base, 8, 128, 256, 256, moe.EPI_SILU_MUL_QUANT, None, None, None, 0, None) == INVALID
     ep = _lib.EpilogueArgs()
     ep.h_scale = 1.0
@@ -124,7 +131,7 @@ def test_grouped_gemm_rejects_before_launch(L):
 def test_finalize_and_forward_reject_before_launch(L):
     assert L.moe_finalize(P, P, P, 4, 2, 12, P, None) == UNSUPPORTED   # N % 8
     assert L.moe_finalize(Q, P, P, 4, 2, 16, P, None) == MISALIGNED
-    w = _lib.Weights(P, P, P, P, P, P)
+    w = _lib.Weights(P, P, P, P)
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 200, 128, 1.0, P, P, 1 << 30, None) == UNSUPPORTED
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 256, 128, 0.0, P, P, 1 << 30, None) == INVALID
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 256, 128, 1.0, P, P, 16, None) == WORKSPACE

@@ -13,7 +13,8 @@ import torch
 import nvfp4_moe_grouped_gb300 as moe
 import oracle
 from nvfp4_moe_grouped_gb300 import inputs
-from tests._helpers import bf16_to_np, counts_to_offsets, padded_rows_of_items, tol_check, untile_rows
+from tests._helpers import (bf16_to_np, counts_to_offsets, padded_rows_of_items, tol_check, unblock_weights,
+                            untile_rows)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -81,19 +82,19 @@ def test_quantize_static_scale_and_zero_rows():
     assert np.array_equal(sf.cpu().numpy(), sf_ref)
 
 
-def test_quantize_weights_grouped_tiled_interleaved_bitexact():
-    E, N, K = 3, 256, 320
+@pytest.mark.parametrize("gate_up,K", [(True, 320), (False, 512), (False, 128)])
+def test_quantize_weights_grouped_blocked_bitexact(gate_up, K):
+    E, N = 3, 256
     w = inputs.expert_weights(E, N, K, 77)
     c_ref, s_ref, sc_ref = oracle.quantize_weights(w.numpy())
-    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=True)
+    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=gate_up)
     torch.cuda.synchronize()
     assert np.array_equal(pw.scale.cpu().numpy(), sc_ref)
-    rowmap = moe.gate_up_row_map(N, "cpu").numpy()
-    codes = pw.codes.cpu().numpy()
+    rowmap = moe.gate_up_row_map(N, "cpu").numpy() if gate_up else np.arange(N)
+    codes, sf = unblock_weights(pw.blocked, E * N, K)
     for e in range(E):
-        assert np.array_equal(codes[e][rowmap], c_ref[e])
-        sf = untile_rows(pw.sf, e * N + rowmap, K)
-        assert np.array_equal(sf, s_ref[e])
+        assert np.array_equal(codes[e * N + rowmap], c_ref[e])
+        assert np.array_equal(sf[e * N + rowmap], s_ref[e])
 
 
 def test_quantize_gather_into_padded_tiled_rows():
