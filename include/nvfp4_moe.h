@@ -149,6 +149,31 @@ MOE_API moe_status moe_route_permute(const float* logits, int T, int E, int k, i
                              int32_t* expanded_to_row, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_route_permute_static -- moe_route_permute without a workspace argument,
+ * for callers that cannot allocate device memory: code running where an
+ * allocation is not allowed or would stall it (cudaMalloc may wait for the
+ * whole device to go idle), or a host whose device memory is all owned by
+ * another allocator.  The pages have no counterpart of this call; it exists
+ * for such callers only.
+ * Same arguments, results and requirements as moe_route_permute, minus
+ * ws/ws_bytes.  Its scratch is one fixed array of
+ * moe_route_permute_static_scratch_bytes() bytes (1 MiB) in the library's
+ * device memory, reserved on every GPU that loads the library until the
+ * process exits; a call whose moe_route_permute_workspace_size(T, E, k)
+ * exceeds it returns MOE_ERR_WORKSPACE without launching anything.  The call
+ * allocates nothing.  The first call on a device looks up the array's device
+ * address (once per device, with that device current); make that first call
+ * before any stream capture.  Every call shares the one array, so calls that
+ * can overlap on the GPU (different streams, or different host threads) race
+ * and must be serialised by the caller.  Nothing in the array needs clearing
+ * between calls: the kernels write every scratch word before they read it.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_route_permute_static_scratch_bytes(void);
+MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, int k, int32_t* topk_id, float* topk_w,
+                                    int32_t* expert_offsets, int32_t* perm_to_expanded, int32_t* expanded_to_perm,
+                                    int32_t* expanded_to_row, void* stream);
+
+/* ---------------------------------------------------------------------------
  * nvfp4_quantize -- NVFP4 quantisation of rows of a bf16 or f32 matrix.
  *   "Cracking the SM120 Shared Memory Ceiling ...", "The Shared Memory
  *   Calculation" (4-bit values, one FP8 scale per 16 elements along K).
