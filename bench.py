@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=T_DEF)
+    ap.add_argument("--experts", type=int, default=E_DEF)
     ap.add_argument("--zipf", type=float, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="layer", choices=["layer", "gemm"],
@@ -80,7 +81,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -221,7 +222,7 @@ def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: bounded samples of the same workload."""
     if rank != 0:
         return
-    T, E, k, H, I = args.tokens, E_DEF, K_DEF, H_DEF, I_DEF
+    T, E, k, H, I = args.tokens, args.experts, K_DEF, H_DEF, I_DEF
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     from nvfp4_moe_grouped_gb300 import inputs
     x = inputs.activations(T, H)
@@ -253,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    T, E, k, H, I = args.tokens, E_DEF, K_DEF, H_DEF, I_DEF
+    T, E, k, H, I = args.tokens, args.experts, K_DEF, H_DEF, I_DEF
     x, logits, pw13, pw2 = make_layer(T, E, k, H, I, args.zipf, dev)
     xd, ld = x.to(dev), logits.to(dev)
     fwd = moe.MoeForward(T, E, k, H, I, dev)
@@ -310,7 +311,7 @@ def run_ours(args, rank, world, local_rank):
         ep.topk_w = f.ptr("topk_w")
         ep.T = T
         ep.k = k
-        wsb = f.lib.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, T, H)
+        wsb = f.lib.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, T, k, H)
         _call("moe_grouped_gemm_nvfp4", f.lib.moe_grouped_gemm_nvfp4(
             f.ptr("h_codes"), f.ptr("h_sf"), f.ptr("h_scale"), _p(w.blocked), _p(w.scale),
             f.ptr("expert_offsets"), E, P, H, I, moe.EPI_FINALIZE, _byref(ep), _p(o), f.ptr("gemm_ws"), wsb, _s()))

@@ -97,7 +97,7 @@ enum { MOE_EPI_NONE = 0, MOE_EPI_SILU_MUL_QUANT = 1, MOE_EPI_FINALIZE = 2 };
 /* Human-readable name of a status code (static string). */
 MOE_API const char* moe_status_string(int status);
 
-/* ABI version of this header; bumped on any incompatible change (2: blocked weights). */
+/* ABI version of this header; bumped on any incompatible change (3: FINALIZE workspace query takes k). */
 MOE_API int moe_abi_version(void);
 
 /* Reads and clears the device error word written by bounded waits that gave
@@ -188,7 +188,10 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
  *                 with its own scale (1 for an activation tensor, E for weights)
  *   tensor_scale  f32 [groups]: in (static) or out (dynamic)
  *   n_items       number of output rows to write
- *   src_div       item i reads source row i / src_div (1 = row i)
+ *   src_div       item i reads source row i / src_div (1 = row i); when
+ *                 src_div > 1 every source row must be read by exactly
+ *                 src_div items (n_items == src_rows * src_div, src_div <= 32):
+ *                 each source row is quantised once and written to all of them
  *   dst_row       i32 [n_items] or NULL: item i is written to output row
  *                 dst_row[i] (NULL: row i)
  *   codes         u8 [dst_rows_alloc][K/2]           out
@@ -229,7 +232,10 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  *     `out` is unused.
  *   MOE_EPI_FINALIZE (down): out = bf16 [ep->T][N],
  *     out[t][n] = sum_j topk_w[t][j] * Y[row of item t*k+j][n], summed in FP32
- *     (atomically: the order of the k terms is not fixed) and rounded once.
+ *     and rounded once.  While T*N*4 bytes <= 64 MiB (an accumulator that
+ *     stays in L2) the sum is FP32 atomics in the epilogue (the order of the k
+ *     terms is not fixed); above that the epilogue stores each item's weighted
+ *     row and a second kernel sums the k rows in slot order.
  * Arguments:
  *   a_codes/a_sf  activations, padded-row layout, tiled scales, a_rows_alloc rows
  *   a_scale       f32 [1] decode multiplier of A
@@ -237,7 +243,8 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  *   b_scale       f32 [E]
  *   expert_offsets i32 [E+1] (as moe_route_permute writes them)
  *   ep            host pointer to epilogue arguments (NULL for NONE)
- *   ws / ws_bytes workspace of moe_grouped_gemm_workspace_size(...) bytes
+ *   ws / ws_bytes workspace of moe_grouped_gemm_workspace_size(epilogue, T, k, N)
+ *                 bytes (FINALIZE only; 0 otherwise)
  * Tiling: the kernel takes 128 weight rows per tile as the MMA M dimension and
  * up to 64 (decode regime: the allocation implies <= 48 routed rows per
  * expert on average) or 128 (otherwise) routed rows as MMA N.
@@ -258,7 +265,7 @@ typedef struct {
   int32_t k;
 } moe_epilogue_args;
 
-MOE_API size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int N);
+MOE_API size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int k, int N);
 MOE_API moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
                                   const uint8_t* b_blocked, const float* b_scale,
                                   const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,

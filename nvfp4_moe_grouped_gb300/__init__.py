@@ -229,7 +229,7 @@ def moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, w: PreparedWeights, expert_of
         ep.topk_w = _ptr(topk_w)
         ep.T = T
         ep.k = k
-        wsb = _L().moe_grouped_gemm_workspace_size(epilogue, T, w.N)
+        wsb = _L().moe_grouped_gemm_workspace_size(epilogue, T, k, w.N)
         ws = _empty(wsb, torch.uint8, dev)
     _check("moe_grouped_gemm_nvfp4", _L().moe_grouped_gemm_nvfp4(
         _ptr(a_codes), _ptr(a_sf), _ptr(a_scale), _ptr(w.blocked), _ptr(w.scale), _ptr(expert_offsets), E,

@@ -63,7 +63,7 @@ SIGNATURES = {
     "nvfp4_quantize_workspace_size": (c_size_t, [c_int]),
     "nvfp4_quantize": (c_int, [c_void_p, c_int, c_int64, c_int, c_int, c_void_p, c_int, c_int64, c_int, c_void_p,
                                c_void_p, c_void_p, c_int, c_int64, c_void_p, c_size_t, c_void_p]),
-    "moe_grouped_gemm_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "moe_grouped_gemm_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
     "moe_grouped_gemm_nvfp4": (c_int, [c_void_p] * 6 + [c_int, c_int64, c_int, c_int, c_int, c_void_p, c_void_p,
                                                         c_void_p, c_size_t, c_void_p]),
     "moe_finalize": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),

@@ -74,19 +74,16 @@ MOE_DEVINL float route_exp(float x) {
 
 // e2m1 code of v: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even
 // code, saturating above 6; a magnitude-0 result is +0.
+// The code is the number of rounding boundaries below |v| (strict at the
+// boundaries that round down to an even code, inclusive at those that round up
+// to one).
 MOE_DEVINL uint32_t e2m1_encode(float v) {
-  float a = fabsf(v);
-  uint32_t c;
-  if (a <= 0.25f) c = 0;
-  else if (a < 0.75f) c = 1;
-  else if (a <= 1.25f) c = 2;
-  else if (a < 1.75f) c = 3;
-  else if (a <= 2.5f) c = 4;
-  else if (a < 3.5f) c = 5;
-  else if (a <= 5.0f) c = 6;
-  else c = 7;
-  if (c != 0 && v < 0.0f) c |= 8u;
-  return c;
+  const float a = fabsf(v);
+  const uint32_t c = static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
+                     static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
+                     static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
+                     static_cast<uint32_t>(a > 5.0f);
+  return (c != 0u && v < 0.0f) ? (c | 8u) : c;
 }
 
 // e4m3 (fn) scale byte of a non-negative value: round to nearest even,
@@ -256,6 +253,19 @@ MOE_DEVINL void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 MOE_DEVINL void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Each thread of the warp stores 32 consecutive 32-bit columns of its lane.
+MOE_DEVINL void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+MOE_DEVINL void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05 format, version 1).
 //   start: byte address; lbo/sbo: leading/stride byte offsets; layout:

@@ -58,7 +58,36 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4* __restri
   }
 }
 
+// out[t][n] = bf16( sum_{j<k} rows[t*k + j][n] ), summed in slot order in FP32.
+__global__ void __launch_bounds__(256) finalize_sum_kernel(const float* __restrict__ rows, int T, int k, int N,
+                                                           uint16_t* __restrict__ out) {
+  const int vec_per_row = N / 4;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= static_cast<int64_t>(T) * vec_per_row) return;
+  const int64_t t = gid / vec_per_row;
+  const int c = static_cast<int>(gid % vec_per_row) * 4;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int j = 0; j < k; ++j) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(rows + (t * k + j) * N + c));
+    acc.x = __fadd_rn(acc.x, v.x);
+    acc.y = __fadd_rn(acc.y, v.y);
+    acc.z = __fadd_rn(acc.z, v.z);
+    acc.w = __fadd_rn(acc.w, v.w);
+  }
+  const uint32_t a = static_cast<uint32_t>(float_to_bf16_bits(acc.x)) | (static_cast<uint32_t>(float_to_bf16_bits(acc.y)) << 16);
+  const uint32_t b = static_cast<uint32_t>(float_to_bf16_bits(acc.z)) | (static_cast<uint32_t>(float_to_bf16_bits(acc.w)) << 16);
+  *reinterpret_cast<uint2*>(out + t * N + c) = make_uint2(a, b);
+}
+
 }  // namespace
+
+moe_status launch_finalize_sum(const float* rows, int T, int k, int N, uint16_t* out, cudaStream_t st) {
+  const int64_t threads = static_cast<int64_t>(T) * (N / 4);
+  const int64_t blocks = (threads + 255) / 256;
+  if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  finalize_sum_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(rows, T, k, N, out);
+  return check_launch();
+}
 
 // Converts n (a multiple of 4) FP32 values to BF16 (round to nearest even).
 moe_status launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t st) {

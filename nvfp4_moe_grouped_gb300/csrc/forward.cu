@@ -38,7 +38,7 @@ extern "C" moe_status moe_forward_workspace_layout(int T, int E, int k, int H, i
   L->h_sf = take(static_cast<size_t>(P) * I / 16);
   L->route_ws = take(moe_route_permute_workspace_size(T, E, k));
   L->quant_ws = take(nvfp4_quantize_workspace_size(1));
-  L->gemm_ws = take(moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, H));
+  L->gemm_ws = take(moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H));
   L->padded_rows = P;
   L->total = o;
   return MOE_OK;
@@ -99,5 +99,5 @@ extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const 
   ep2.k = k;
   return moe_grouped_gemm_nvfp4(h_codes, h_sf, hs, w->w2, w->w2_scale, offs, E, L.padded_rows, H, I,
                                 MOE_EPI_FINALIZE, &ep2, out, at(L.gemm_ws),
-                                moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, H), stream);
+                                moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H), stream);
 }

@@ -31,12 +31,16 @@
 //     streams a contiguous 18 KB run of HBM.
 //   * Warp roles: warp 0 issues the copies (weights: bulk copy, evict-first;
 //     routed rows: 2D tensor-map loads of 32 rows with 128-byte swizzle and
-//     a bulk copy of their scale atoms, evict-last), warp 1 owns tensor memory
-//     and issues tcgen05.cp (scales -> TMEM) and tcgen05.mma, warps 2-5 drain
-//     the accumulator (tcgen05.ld) and run the epilogue.  Two TMEM
-//     accumulators let the epilogue of one unit overlap the mainloop of the
-//     next; every stage has its own TMEM scale slot, recycled by the same
-//     commit that frees the stage.
+//     a bulk copy of their scale atoms, evict-last), warps 6-9 move each
+//     stage's scale atoms from shared into tensor memory (tcgen05.st, one
+//     warp per lane quadrant), warp 1 owns tensor memory and issues only the
+//     tcgen05.mma instructions and their commits, warps 2-5 drain the
+//     accumulator (tcgen05.ld) and run the epilogue.  A tcgen05.cp of the
+//     scales on the MMA thread would serialise with the MMA that reads them:
+//     at decode that halved the weight-streaming rate.  Two TMEM accumulators
+//     let the epilogue of one unit overlap the mainloop of the next; every
+//     stage has its own TMEM scale slot, recycled by the same commit that
+//     frees the stage.
 //   * Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT in the
 //     device error word, lets its own copies and MMAs finish, frees its tensor
 //     memory and returns.
@@ -44,6 +48,14 @@
 
 namespace moe {
 moe_status launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t st);
+moe_status launch_finalize_sum(const float* rows, int T, int k, int N, uint16_t* out, cudaStream_t st);
+
+// FINALIZE accumulates with atomics into a [T][N] FP32 buffer while that buffer
+// fits comfortably in L2; above this size every atomic would miss to HBM, so the
+// epilogue instead stores each expanded item's weighted row and a second kernel
+// sums the k rows of every token (deterministically, in slot order).
+constexpr int64_t kFinalizeAtomicMaxBytes = 64ll << 20;
+inline bool finalize_gathers(int T, int N) { return static_cast<int64_t>(T) * N * 4 > kFinalizeAtomicMaxBytes; }
 
 namespace {
 
@@ -51,10 +63,11 @@ constexpr int kBM = 128;                  // weight rows per tile (MMA M)
 constexpr int kBK = 256;                  // K elements per stage (128 bytes per row)
 constexpr int kWStageBytes = kBlockedTileBytes;  // 16 KB codes + 2 KB scale atoms
 constexpr int kSfStageBytes = 4 * 512;    // scale atoms of the routed rows (one per 64-element K step)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warp 0 copies, 1 MMA, 2-5 epilogue, 6-9 scale staging
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfSlotCols = 32;      // 16 columns weight scales + 16 columns routed-row scales
+constexpr int kEpiStride = 129;           // floats per staged routed row (128 tile rows + 1 against bank conflicts)
 
 template <int BN>
 struct Cfg {
@@ -67,11 +80,11 @@ struct Cfg {
   static constexpr int w = 0;
   static constexpr int x = w + kStages * kWStageBytes;
   static constexpr int sfx = x + kStages * kXStageBytes;
-  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][65]
-  static constexpr int tok_t = epi + 32 * 65 * 4;            // int [BN]
+  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][kEpiStride]
+  static constexpr int tok_t = epi + 32 * kEpiStride * 4;    // int [BN]
   static constexpr int tok_w = tok_t + BN * 4;               // float [BN]
-  static constexpr int bars = tok_w + BN * 4;                // uint64 [2*kStages + 5]
-  static constexpr int misc = bars + (2 * kStages + 5) * 8;  // tmem base, abort flag
+  static constexpr int bars = tok_w + BN * 4;                // uint64 [3*kStages + 5]
+  static constexpr int misc = bars + (3 * kStages + 5) * 8;  // tmem base, abort flag
   static constexpr int sched = misc + 16;                    // int [3][kMaxExperts+1]
   static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
   static constexpr int smem_bytes = total + 1024;            // + alignment slack
@@ -87,7 +100,7 @@ struct GemmParams {
   const int32_t* expert_offsets;
   int E, N, K;
   int epilogue;
-  void* out;                  // NONE: bf16 [rows][N]; FINALIZE: f32 accumulator [T][N]
+  void* out;                  // NONE: bf16 [rows][N]; FINALIZE: f32 [T][N] accumulator or [T*k][N] rows
   float h_scale;
   float* h_scale_out;
   uint8_t* h_codes;
@@ -97,6 +110,7 @@ struct GemmParams {
   const float* topk_w;
   int k;
   int T;
+  int fin_gather;             // FINALIZE: 1 = store weighted rows per expanded item (summed later), 0 = atomics
   int64_t rows_alloc;         // rows of the routed-row operand (bounds every access to it)
   int32_t* err;
   uint64_t timeout_ns;
@@ -167,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_tok_w = reinterpret_cast<float*>(smem + C::tok_w);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bars);
   uint64_t* empty = full + S;
-  uint64_t* acc_full = empty + S;
+  uint64_t* sf_ready = empty + S;
+  uint64_t* acc_full = sf_ready + S;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::misc);
@@ -183,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- prologue: barriers, tensor memory, work list --------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sf_ready[s], 4); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
     mbar_init(mma_done, 1);
     *s_abort = 0;
@@ -300,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (x_row % 128) / 32 TMEM columns into each atom's four columns.
         const uint32_t sfx_col_off = static_cast<uint32_t>((d.x_row & 127) >> 5);
         for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort)) {
+          // sf_ready implies full: the staging warps saw the stage's copies land.
+          if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 3);
             *s_abort = 1;
             ok = false;
@@ -310,12 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int steps = min(4, (K - kt * kBK) / 64);
           const uint32_t sf_col = tmem_base + C::kSfTmemBase + stage * kSfSlotCols;
           const uint32_t w_addr = smem_u32(s_w + stage * kWStageBytes);
-          const uint32_t sfw_addr = w_addr + 16384;
-          const uint32_t sfx_addr = smem_u32(s_sfx + stage * kSfStageBytes);
-          for (int g = 0; g < steps; ++g) {
-            tmem_cp_32x128b_x4(sf_col + 4 * g, smem_desc(sfw_addr + 512 * g, 0, 128, 0));
-            tmem_cp_32x128b_x4(sf_col + 16 + 4 * g, smem_desc(sfx_addr + 512 * g, 0, 128, 0));
-          }
           const uint32_t x_addr = smem_u32(s_x + stage * C::kXStageBytes);
           for (int g = 0; g < steps; ++g) {
             const uint64_t adesc = smem_desc(w_addr + 32 * g, 16, 1024, 2);
@@ -333,6 +343,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(mma_done);
       int zero = 0;
       mbar_wait_bounded(mma_done, 0, p.timeout_ns, reinterpret_cast<volatile int*>(&zero));
+    }
+  } else if (warp >= 6) {
+    // ---------------- scale staging warps 6..9 ----------------
+    // The block-scaled MMA reads its scales from tensor memory.  Each of these
+    // warps (one per TMEM lane quadrant) writes the stage's 32 scale columns
+    // into its quadrant: columns 0-15 the weight atoms of the 4 K steps,
+    // columns 16-31 the routed-row atoms, each atom's 32 rows of 16 bytes in
+    // lanes 0-31 of every quadrant.  Keeping these stores off the MMA thread
+    // leaves it nothing to issue but the MMAs themselves.
+    const uint32_t quad_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+      if (!d.valid) continue;
+      for (int kt = 0; kt < KT; ++kt) {
+        const bool got = mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) {
+            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 7);
+            *s_abort = 1;
+          }
+          ok = false;
+          break;
+        }
+        const uint8_t* sfw = s_w + stage * kWStageBytes + 16384 + lane * 16;
+        const uint8_t* sfx = s_sfx + stage * kSfStageBytes + lane * 16;
+        uint32_t v[32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sfw + 512 * g);
+          const uint4 b = *reinterpret_cast<const uint4*>(sfx + 512 * g);
+          v[4 * g] = a.x; v[4 * g + 1] = a.y; v[4 * g + 2] = a.z; v[4 * g + 3] = a.w;
+          v[16 + 4 * g] = b.x; v[16 + 4 * g + 1] = b.y; v[16 + 4 * g + 2] = b.z; v[16 + 4 * g + 3] = b.w;
+        }
+        tmem_st_32cols(tmem_base + quad_lane + C::kSfTmemBase + stage * kSfSlotCols, v);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[stage]);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
     }
   } else {
     // ---------------- epilogue warps 2..5 ----------------
@@ -368,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ex = __ldg(p.perm_to_expanded + d.m_off + et);
           const bool in_range = ex >= 0 && ex < p.T * p.k;
           if (!in_range) record_error(p.err, MOE_ERR_INVALID_ARG, 6);
-          s_tok_t[et] = in_range ? ex / p.k : -1;
+          s_tok_t[et] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
           s_tok_w[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
         }
         epi_bar();
@@ -389,38 +442,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (p.epilogue == MOE_EPI_FINALIZE) {
           float* acc = static_cast<float*>(p.out);
           const int64_t col = static_cast<int64_t>(d.mt) * kBM + m;
+          if (p.fin_gather) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
-            if (jj < jn && s_tok_t[j0 + jj] >= 0)
-              atomicAdd(acc + static_cast<int64_t>(s_tok_t[j0 + jj]) * N + col,
-                        s_tok_w[j0 + jj] * __uint_as_float(r[jj]));
+            for (int jj = 0; jj < 32; ++jj)
+              if (jj < jn && s_tok_t[j0 + jj] >= 0)
+                acc[static_cast<int64_t>(s_tok_t[j0 + jj]) * N + col] = s_tok_w[j0 + jj] * __uint_as_float(r[jj]);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              if (jj < jn && s_tok_t[j0 + jj] >= 0)
+                atomicAdd(acc + static_cast<int64_t>(s_tok_t[j0 + jj]) * N + col,
+                          s_tok_w[j0 + jj] * __uint_as_float(r[jj]));
+          }
         } else {
           // gate_up tile: rows 0-63 are gate rows, rows 64-127 the matching up rows.
+          // Stage the chunk (128 tile rows x 32 routed rows) in shared memory, then
+          // give each thread one routed row and one 16-wide block of the 64 outputs,
+          // so an NVFP4 block (amax, scale, codes) lives in one thread's registers.
           const int I = N / 2;
-          if (q >= 2) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) s_epi[jj * 65 + (m - 64)] = alpha * __uint_as_float(r[jj]);
-          }
+          for (int jj = 0; jj < 32; ++jj) s_epi[jj * kEpiStride + m] = alpha * __uint_as_float(r[jj]);
           epi_bar();
-          if (q < 2) {
-            const int i = d.mt * 64 + m;
+          const int jj = et >> 2, blk = et & 3;
+          if (jj < jn) {
+            const float* gp = s_epi + jj * kEpiStride + 16 * blk;
+            float h[16];
+            float amax = 0.0f;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              if (jj >= jn) break;  // jn is the same on every lane
-              const float g = alpha * __uint_as_float(r[jj]);
-              const float up = s_epi[jj * 65 + m];
-              const float h = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), up);
-              const int64_t row = d.x_row + j0 + jj;
-              if (p.h_f32) p.h_f32[row * I + i] = h;
-              float amax = fabsf(h);
+            for (int t = 0; t < 16; ++t) {
+              const float g = gp[t];
+              h[t] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), gp[64 + t]);
+              amax = fmaxf(amax, fabsf(h[t]));
+            }
+            float recip;
+            const uint32_t sfb = nvfp4_block_scale(amax, p.h_scale, &recip);
+            uint32_t lo = 0, hi = 0;
 #pragma unroll
-              for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-              float recip;
-              const uint32_t sfb = nvfp4_block_scale(amax, p.h_scale, &recip);
-              const uint32_t code = nvfp4_code(h, recip);
-              const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
-              if ((lane & 1) == 0) p.h_codes[row * (I / 2) + i / 2] = static_cast<uint8_t>(code | (hi << 4));
-              if ((lane & 15) == 0) p.h_sf[tiled_sf_offset(row, i / 16, I)] = static_cast<uint8_t>(sfb);
+            for (int t = 0; t < 8; ++t) lo |= nvfp4_code(h[t], recip) << (4 * t);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) hi |= nvfp4_code(h[8 + t], recip) << (4 * t);
+            const int64_t row = d.x_row + j0 + jj;
+            const int i0 = d.mt * 64 + 16 * blk;
+            *reinterpret_cast<uint2*>(p.h_codes + row * (I / 2) + i0 / 2) = make_uint2(lo, hi);
+            p.h_sf[tiled_sf_offset(row, i0 / 16, I)] = static_cast<uint8_t>(sfb);
+            if (p.h_f32) {
+              float4* dst = reinterpret_cast<float4*>(p.h_f32 + row * I + i0);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) dst[t] = make_float4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
             }
           }
           epi_bar();
@@ -512,10 +580,11 @@ int gemm_tile_rows(int64_t a_rows_alloc, int E) {
 
 using namespace moe;
 
-extern "C" size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int N) {
+extern "C" size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int k, int N) {
   if (epilogue != MOE_EPI_FINALIZE) return 0;
-  if (T < 1 || N < 1) return 0;
+  if (T < 1 || N < 1 || k < 1) return 0;
   size_t b = static_cast<size_t>(T) * N * sizeof(float);
+  if (finalize_gathers(T, N)) b *= static_cast<size_t>(k);
   return ((b + 255) / 256) * 256;
 }
 
@@ -557,13 +626,14 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   } else {
     if (!ep || !ep->perm_to_expanded || !ep->topk_w || !out || ep->T < 1 || ep->k < 1) return MOE_ERR_INVALID_ARG;
     if (!aligned16(out)) return MOE_ERR_MISALIGNED;
-    if (!ws || ws_bytes < moe_grouped_gemm_workspace_size(epilogue, ep->T, N)) return MOE_ERR_WORKSPACE;
+    if (!ws || ws_bytes < moe_grouped_gemm_workspace_size(epilogue, ep->T, ep->k, N)) return MOE_ERR_WORKSPACE;
     if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
     p.out = ws;
     p.perm_to_expanded = ep->perm_to_expanded;
     p.topk_w = ep->topk_w;
     p.k = ep->k;
     p.T = ep->T;
+    p.fin_gather = finalize_gathers(ep->T, N) ? 1 : 0;
   }
   p.rows_alloc = a_rows_alloc;
   p.err = device_error_word();
@@ -574,7 +644,7 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   CUtensorMap tm_x;
   if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (epilogue == MOE_EPI_FINALIZE) {
+  if (epilogue == MOE_EPI_FINALIZE && !p.fin_gather) {
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
@@ -582,8 +652,11 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
   moe_status s = bn == 64 ? launch_gemm<64>(tm_x, p, max_units, st) : launch_gemm<128>(tm_x, p, max_units, st);
   if (s != MOE_OK) return s;
-  if (epilogue == MOE_EPI_FINALIZE)
+  if (epilogue == MOE_EPI_FINALIZE) {
+    if (p.fin_gather)
+      return launch_finalize_sum(static_cast<const float*>(ws), ep->T, ep->k, N, static_cast<uint16_t*>(out), st);
     return launch_f32_to_bf16(static_cast<const float*>(ws), static_cast<uint16_t*>(out),
                               static_cast<int64_t>(ep->T) * N, st);
+  }
   return MOE_OK;
 }

@@ -16,6 +16,7 @@ namespace moe {
 namespace {
 
 constexpr int kQuantWarps = 8;
+constexpr int kMaxFan = 32;  // largest number of items one source row fans out to (the top-k bound)
 
 template <int IN_F32>
 MOE_DEVINL void load_block16(const void* x, int64_t row, int K, int blk, float (&v)[16]) {
@@ -91,15 +92,23 @@ MOE_DEVINL void block_dst(uint8_t* codes, uint8_t* sf, int64_t dst, int c, int K
   }
 }
 
+// One warp per source row.  The row is quantised once and written to every
+// item that reads it: items [src * fan, src * fan + fan) when fan > 1 (all
+// items of a source row are consecutive when items map to rows i / src_div),
+// or the single item `src` when fan == 1.
 template <int IN_F32, int LAYOUT>
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
-    const void* __restrict__ x, int64_t rows_per_group, int K, const float* __restrict__ scale, int64_t n_items,
-    int src_div, const int32_t* __restrict__ dst_row, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+    const void* __restrict__ x, int64_t rows_per_group, int K, const float* __restrict__ scale, int64_t n_src,
+    int fan, const int32_t* __restrict__ dst_row, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
-  if (item >= n_items) return;
-  const int64_t src = item / src_div;
-  const int64_t dst = dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item;
+  const int64_t src = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (src >= n_src) return;
+  int64_t dst[kMaxFan];
+#pragma unroll
+  for (int j = 0; j < kMaxFan; ++j) {
+    const int64_t item = src * fan + j;
+    dst[j] = (j < fan) ? (dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item) : 0;
+  }
   const float s = __ldg(scale + src / rows_per_group);
   const int nblk = K / 16;
   for (int c = lane; c < nblk; c += 32) {
@@ -115,10 +124,14 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
     for (int i = 0; i < 8; ++i) lo |= nvfp4_code(v[i], recip) << (4 * i);
 #pragma unroll
     for (int i = 0; i < 8; ++i) hi |= nvfp4_code(v[8 + i], recip) << (4 * i);
-    uint8_t *code_at, *sf_at;
-    block_dst<LAYOUT>(codes, sf, dst, c, K, &code_at, &sf_at);
-    *reinterpret_cast<uint2*>(code_at) = make_uint2(lo, hi);
-    *sf_at = static_cast<uint8_t>(sfb);
+#pragma unroll
+    for (int j = 0; j < kMaxFan; ++j) {
+      if (j >= fan) break;
+      uint8_t *code_at, *sf_at;
+      block_dst<LAYOUT>(codes, sf, dst[j], c, K, &code_at, &sf_at);
+      *reinterpret_cast<uint2*>(code_at) = make_uint2(lo, hi);
+      *sf_at = static_cast<uint8_t>(sfb);
+    }
   }
 }
 
@@ -152,6 +165,8 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
   if (src_rows % groups) return MOE_ERR_INVALID_ARG;
   if ((n_items - 1) / src_div >= src_rows && n_items > 0) return MOE_ERR_INVALID_ARG;
   if (!dst_row && n_items > dst_rows_alloc) return MOE_ERR_INVALID_ARG;
+  // A source row read by several items is quantised once and fanned out to all of them.
+  if (src_div > 1 && (src_div > 32 || n_items != src_rows * src_div)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(codes) || (sf && !aligned16(sf))) return MOE_ERR_MISALIGNED;
   if (dynamic_scale && (!ws || ws_bytes < nvfp4_quantize_workspace_size(groups))) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -171,12 +186,17 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
     scale_from_amax_kernel<<<(groups + 255) / 256, 256, 0, st>>>(amax, groups, tensor_scale);
   }
   if (n_items > 0) {
-    int64_t blocks = (n_items + kQuantWarps - 1) / kQuantWarps;
+    // Fan out when every source row is read by src_div consecutive items (the
+    // routed-row gather); otherwise one item per warp.
+    const bool fan_out = src_div > 1;
+    const int fan = fan_out ? src_div : 1;
+    const int64_t n_src = fan_out ? src_rows : n_items;
+    int64_t blocks = (n_src + kQuantWarps - 1) / kQuantWarps;
     if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
     const bool f32 = in_dtype == MOE_IN_F32;
 #define MOE_QLAUNCH(F, T)                                                                                     \
   quantize_kernel<F, T><<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, st>>>(                          \
-      x, rows_per_group, K, tensor_scale, n_items, src_div, dst_row, codes, sf)
+      x, rows_per_group, K, tensor_scale, n_src, fan, dst_row, codes, sf)
     if (f32) {
       if (sf_layout == MOE_SF_BLOCKED) MOE_QLAUNCH(1, 2);
       else if (sf_layout == MOE_SF_TILED) MOE_QLAUNCH(1, 1);

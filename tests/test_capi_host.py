@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.moe_abi_version() == 2
+    assert L.moe_abi_version() == 3
     for s in range(8):
         assert L.moe_status_string(s)
     assert L.moe_status_string(99) == b"unknown status"
@@ -72,8 +72,9 @@ def test_blocked_weight_bytes(L):
 
 
 def test_workspace_queries(L):
-    assert L.moe_grouped_gemm_workspace_size(moe.EPI_NONE, 1024, 6144) == 0
-    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 1024, 6144) == 1024 * 6144 * 4
+    assert L.moe_grouped_gemm_workspace_size(moe.EPI_NONE, 1024, 8, 6144) == 0
+    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 1024, 8, 6144) == 1024 * 6144 * 4      # atomics
+    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 16384, 8, 6144) == 16384 * 8 * 6144 * 4  # rows
     assert L.nvfp4_quantize_workspace_size(1) == 256
     assert L.moe_route_permute_workspace_size(1024, 256, 8) >= (1024 // 32) * 256 * 4
 
