@@ -57,6 +57,30 @@ def parse():
     return ap.parse_args()
 
 
+def kernel_source_digest() -> str:
+    """SHA-256 of the grouped-GEMM source and the headers it includes (identifies the measured kernel)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in ("nvfp4_moe_grouped_gb300/csrc/grouped_gemm.cu", "nvfp4_moe_grouped_gb300/csrc/common.cuh",
+                "include/nvfp4_moe.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the gate_up GEMM from the committed ncu record, or None when the record is
+    for another workload or for a kernel source that has changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.json")) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("workload") != workload or rec.get("kernel_sha256") != kernel_source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -421,6 +445,7 @@ def run_ours(args, rank, world, local_rank):
         return
 
     hbm_peak, bf16_peak, peak_kind = peaks()
+    workload = f"moe_layer_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf else "_uniform")
     gate_up_ms = stage_ms[2]
     flops_gate_up = 2.0 * T * k * 2 * I * H
     fp4_peak = moe.fp4_mma_peak_tflops()
@@ -437,7 +462,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = ab["gate_up"] / (gate_up_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "peak_kind": peak_kind, "traffic": None,
+                "peak_kind": peak_kind, "traffic": recorded_traffic(workload),
                 "algorithmic_bytes_per_launch": ab["gate_up"], "launch_ms": gate_up_ms}
     flops_layer = 2.0 * T * k * (2 * I * H + H * I)
     cpu = None
@@ -450,7 +475,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1xe2m1->f32", "data": "synthetic",
-        "config": {"workload": f"moe_layer_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf else "_uniform"),
+        "config": {"workload": workload,
                    "tokens": T, "experts": E, "top_k": k, "hidden": H, "intermediate": I,
                    "l2": "weights (5.4 GB) exceed L2; no flush", "parallelism": f"replicas{world}"},
         "roofline": roof,

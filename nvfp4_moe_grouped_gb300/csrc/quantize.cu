@@ -16,7 +16,6 @@ namespace moe {
 namespace {
 
 constexpr int kQuantWarps = 8;
-constexpr int kMaxFan = 32;  // largest number of items one source row fans out to (the top-k bound)
 
 template <int IN_F32>
 MOE_DEVINL void load_block16(const void* x, int64_t row, int K, int blk, float (&v)[16]) {
@@ -92,10 +91,34 @@ MOE_DEVINL void block_dst(uint8_t* codes, uint8_t* sf, int64_t dst, int c, int K
   }
 }
 
+// Quantises one 16-element block: codes of elements 0-7 in *lo, 8-15 in *hi
+// (element 2i in the low nibble of byte i), returns the e4m3 scale byte.
+template <int IN_F32>
+MOE_DEVINL uint32_t quantize_block16(const void* x, int64_t row, int K, int blk, float s, uint32_t* lo,
+                                     uint32_t* hi) {
+  float v[16];
+  load_block16<IN_F32>(x, row, K, blk, v);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  float recip;
+  const uint32_t sfb = nvfp4_block_scale(amax, s, &recip);
+  uint32_t l = 0, h = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) l |= nvfp4_code(v[i], recip) << (4 * i);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h |= nvfp4_code(v[8 + i], recip) << (4 * i);
+  *lo = l;
+  *hi = h;
+  return sfb;
+}
+
 // One warp per source row.  The row is quantised once and written to every
 // item that reads it: items [src * fan, src * fan + fan) when fan > 1 (all
 // items of a source row are consecutive when items map to rows i / src_div),
-// or the single item `src` when fan == 1.
+// or the single item `src` when fan == 1.  When K % 64 == 0 each lane owns 4
+// consecutive blocks (64 elements), so every destination gets 32 bytes of
+// codes and 4 contiguous scale bytes (one aligned word in every layout).
 template <int IN_F32, int LAYOUT>
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
     const void* __restrict__ x, int64_t rows_per_group, int K, const float* __restrict__ scale, int64_t n_src,
@@ -103,34 +126,47 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t src = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
   if (src >= n_src) return;
-  int64_t dst[kMaxFan];
-#pragma unroll
-  for (int j = 0; j < kMaxFan; ++j) {
-    const int64_t item = src * fan + j;
-    dst[j] = (j < fan) ? (dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item) : 0;
-  }
   const float s = __ldg(scale + src / rows_per_group);
-  const int nblk = K / 16;
-  for (int c = lane; c < nblk; c += 32) {
-    float v[16];
-    load_block16<IN_F32>(x, src, K, c, v);
-    float amax = 0.0f;
+  if (K % 64 == 0) {
+    for (int q = lane; q < K / 64; q += 32) {
+      uint32_t c[8];
+      uint32_t sf4 = 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    float recip;
-    uint32_t sfb = nvfp4_block_scale(amax, s, &recip);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) lo |= nvfp4_code(v[i], recip) << (4 * i);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) hi |= nvfp4_code(v[8 + i], recip) << (4 * i);
-#pragma unroll
-    for (int j = 0; j < kMaxFan; ++j) {
-      if (j >= fan) break;
-      uint8_t *code_at, *sf_at;
-      block_dst<LAYOUT>(codes, sf, dst[j], c, K, &code_at, &sf_at);
-      *reinterpret_cast<uint2*>(code_at) = make_uint2(lo, hi);
-      *sf_at = static_cast<uint8_t>(sfb);
+      for (int b = 0; b < 4; ++b) sf4 |= quantize_block16<IN_F32>(x, src, K, 4 * q + b, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
+      for (int j = 0; j < fan; ++j) {
+        const int64_t item = src * fan + j;
+        const int64_t dst = dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item;
+        uint8_t *c0, *c1, *sf_at;
+        if (LAYOUT == 2) {
+          const int kt_count = (K + 255) / 256;
+          const int rr = static_cast<int>(dst & 127);
+          uint8_t* base = codes + ((dst >> 7) * kt_count + (q >> 2)) * static_cast<int64_t>(kBlockedTileBytes);
+          const int chunk = 2 * (q & 3);
+          c0 = base + rr * 128 + ((chunk ^ (rr & 7)) << 4);
+          c1 = base + rr * 128 + (((chunk + 1) ^ (rr & 7)) << 4);
+          sf_at = base + 16384 + (q & 3) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+        } else {
+          c0 = codes + dst * (K / 2) + 32 * q;
+          c1 = c0 + 16;
+          sf_at = (LAYOUT == 1) ? sf + tiled_sf_offset(dst, 4 * q, K) : sf + dst * (K / 16) + 4 * q;
+        }
+        *reinterpret_cast<uint4*>(c0) = make_uint4(c[0], c[1], c[2], c[3]);
+        *reinterpret_cast<uint4*>(c1) = make_uint4(c[4], c[5], c[6], c[7]);
+        *reinterpret_cast<uint32_t*>(sf_at) = sf4;
+      }
+    }
+  } else {
+    for (int blk = lane; blk < K / 16; blk += 32) {
+      uint32_t lo, hi;
+      const uint32_t sfb = quantize_block16<IN_F32>(x, src, K, blk, s, &lo, &hi);
+      for (int j = 0; j < fan; ++j) {
+        const int64_t item = src * fan + j;
+        const int64_t dst = dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item;
+        uint8_t *code_at, *sf_at;
+        block_dst<LAYOUT>(codes, sf, dst, blk, K, &code_at, &sf_at);
+        *reinterpret_cast<uint2*>(code_at) = make_uint2(lo, hi);
+        *sf_at = static_cast<uint8_t>(sfb);
+      }
     }
   }
 }

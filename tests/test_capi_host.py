@@ -103,6 +103,8 @@ def test_quantize_rejects_before_launch(L):
     assert q(Q, 0, 16, 64, 1, P, 0, 16, 1, None, P, P, 0, 16, P, 256, None) == MISALIGNED
     assert q(P, 0, 16, 64, 1, P, 1, 16, 1, None, P, P, 0, 16, None, 0, None) == WORKSPACE
     assert q(P, 7, 16, 64, 1, P, 0, 16, 1, None, P, P, 0, 16, P, 256, None) == INVALID         # dtype
+    assert q(P, 0, 16, 64, 1, P, 0, 30, 2, P, P, P, 0, 32, P, 256, None) == UNSUPPORTED       # partial fan-out
+    assert q(P, 0, 2, 64, 1, P, 0, 66, 33, P, P, P, 0, 66, P, 256, None) == UNSUPPORTED       # fan-out > 32
 
 
 def test_grouped_gemm_rejects_before_launch(L):
