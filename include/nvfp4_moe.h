@@ -333,6 +333,32 @@ MOE_API moe_status moe_forward_workspace_layout(int T, int E, int k, int H, int 
 MOE_API moe_status moe_forward(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k, int H,
                        int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * moe_forward_graph_* -- the whole layer as one CUDA graph.
+ *   "Tracing the Failure ...", "Conclusion" names persistent kernel designs as
+ *   the way past per-kernel overheads; "The Epilogue That Broke the Kernel
+ *   ...", "The Broader Significance" names piecewise CUDA graphs.
+ * moe_forward_graph_create checks its arguments like moe_forward, runs the
+ * layer once eagerly (which computes `out` and prepares every kernel), then
+ * captures moe_forward's launches into an executable graph.  The graph keeps
+ * every pointer it was created with: refill x and logits in place and
+ * relaunch; the workspace, weights and out must stay valid and must not be
+ * used by anything else while a launch of the graph may run.  With
+ * stage_events != 0 the graph records timing events between the four stages
+ * (route+permute, quantise x, gate_up GEMM, down GEMM + FINALIZE);
+ * moe_forward_graph_stage_ms waits for the last launch and writes the five
+ * durations in ms (the four stages, then the whole layer) to ms[5] (host).
+ * Creation makes CUDA objects (a stream, events, the executable graph) but no
+ * device buffers; destroy releases them.  *graph (host) receives the handle.
+ * ------------------------------------------------------------------------- */
+typedef struct moe_forward_graph moe_forward_graph;
+MOE_API moe_status moe_forward_graph_create(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E,
+                                    int k, int H, int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes,
+                                    int stage_events, moe_forward_graph** graph);
+MOE_API moe_status moe_forward_graph_launch(moe_forward_graph* graph, void* stream);
+MOE_API moe_status moe_forward_graph_stage_ms(moe_forward_graph* graph, float* ms);
+MOE_API void moe_forward_graph_destroy(moe_forward_graph* graph);
+
 #ifdef __cplusplus
 }
 #endif

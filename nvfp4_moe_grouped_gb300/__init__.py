@@ -27,7 +27,7 @@ SF_LINEAR, SF_TILED, SF_BLOCKED = 0, 1, 2
 __all__ = ["moe_route_permute", "nvfp4_quantize", "moe_grouped_gemm_nvfp4", "moe_finalize", "moe_forward",
            "prepare_expert_weights", "MoeForward", "padded_rows_max", "device_error", "EPI_NONE",
            "EPI_SILU_MUL_QUANT", "EPI_FINALIZE", "SF_LINEAR", "SF_TILED", "SF_BLOCKED", "MoeError",
-           "EpilogueArgs"]
+           "EpilogueArgs", "ForwardGraph"]
 
 
 def _L():
@@ -270,6 +270,12 @@ class MoeForward:
         nbytes = n * torch.empty((), dtype=dtype).element_size()
         return self.ws[off:off + nbytes].view(dtype).view(shape)
 
+    def graph(self, x, logits, w13: PreparedWeights, w2: PreparedWeights, h_scale: float, out=None,
+              stage_events: bool = True) -> "ForwardGraph":
+        if out is None:
+            out = _empty((self.T, self.H), torch.bfloat16, x.device)
+        return ForwardGraph(self, x, logits, w13, w2, h_scale, out, stage_events)
+
     def __call__(self, x, logits, w13: PreparedWeights, w2: PreparedWeights, h_scale: float, out=None, stream=None):
         if out is None:
             out = _empty((self.T, self.H), torch.bfloat16, x.device)
@@ -278,6 +284,44 @@ class MoeForward:
             _ptr(x), _ptr(logits), ctypes.byref(wts), self.T, self.E, self.k, self.H, self.I, float(h_scale),
             _ptr(out), _ptr(self.ws), self.layout.total, _stream(stream)))
         return out
+
+
+class ForwardGraph:
+    """The whole layer captured as one CUDA graph (see moe_forward_graph_create).
+
+    It keeps the tensors it was created with; refill x and logits in place and call launch().
+    """
+
+    def __init__(self, fwd: "MoeForward", x, logits, w13: PreparedWeights, w2: PreparedWeights, h_scale: float, out,
+                 stage_events: bool = True):
+        self._keep = (fwd, x, logits, w13, w2, out)
+        self.out = out
+        self.handle = ctypes.c_void_p(None)
+        wts = Weights(_ptr(w13.blocked), _ptr(w13.scale), _ptr(w2.blocked), _ptr(w2.scale))
+        _check("moe_forward_graph_create", _L().moe_forward_graph_create(
+            _ptr(x), _ptr(logits), ctypes.byref(wts), fwd.T, fwd.E, fwd.k, fwd.H, fwd.I, float(h_scale), _ptr(out),
+            _ptr(fwd.ws), fwd.layout.total, int(stage_events), ctypes.byref(self.handle)))
+
+    def launch(self, stream=None):
+        _check("moe_forward_graph_launch", _L().moe_forward_graph_launch(self.handle, _stream(stream)))
+        return self.out
+
+    def stage_ms(self):
+        """(route, quantise, gate_up, down+finalize, total) of the last launch, in ms."""
+        ms = (ctypes.c_float * 5)()
+        _check("moe_forward_graph_stage_ms", _L().moe_forward_graph_stage_ms(self.handle, ms))
+        return list(ms)
+
+    def close(self):
+        if self.handle:
+            _L().moe_forward_graph_destroy(self.handle)
+            self.handle = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def moe_forward(x, logits, w13: PreparedWeights, w2: PreparedWeights, k: int, h_scale: float, out=None, stream=None):

@@ -72,6 +72,11 @@ SIGNATURES = {
     "moe_forward_workspace_layout": (c_int, [c_int] * 5 + [c_void_p]),
     "moe_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,
                             c_void_p, c_size_t, c_void_p]),
+    "moe_forward_graph_create": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
+                                         c_void_p, c_void_p, c_size_t, c_int, c_void_p]),
+    "moe_forward_graph_launch": (c_int, [c_void_p, c_void_p]),
+    "moe_forward_graph_stage_ms": (c_int, [c_void_p, c_void_p]),
+    "moe_forward_graph_destroy": (None, [c_void_p]),
 }
 
 _lib = None

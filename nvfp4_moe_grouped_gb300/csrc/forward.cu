@@ -50,20 +50,39 @@ extern "C" size_t moe_forward_workspace_size(int T, int E, int k, int H, int I) 
   return L.total;
 }
 
-extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k,
-                                  int H, int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes,
-                                  void* stream) {
+namespace {
+
+// Checks everything the stage calls would check, so moe_forward either fails
+// before enqueueing anything or enqueues the whole layer.
+moe_status forward_check(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k, int H,
+                         int I, float h_scale, const uint16_t* out, const void* ws, size_t ws_bytes,
+                         moe_forward_layout* L) {
   if (!x || !logits || !w || !out) return MOE_ERR_INVALID_ARG;
   if (!w->w13 || !w->w13_scale || !w->w2 || !w->w2_scale) return MOE_ERR_INVALID_ARG;
   if (T < 1 || E < 1 || k < 1 || k > E || H < 1 || I < 1 || !(h_scale > 0.0f)) return MOE_ERR_INVALID_ARG;
-  if (H % 128 || I % 64) return MOE_ERR_UNSUPPORTED;
-  moe_forward_layout L;
-  moe_status s = moe_forward_workspace_layout(T, E, k, H, I, &L);
+  if (H % 128 || I % 64 || E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  moe_status s = moe_forward_workspace_layout(T, E, k, H, I, L);
   if (s != MOE_OK) return s;
-  if (!ws || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  if (!aligned16(ws)) return MOE_ERR_MISALIGNED;
+  if (!ws || ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws) || !aligned16(x) || !aligned16(out) || !aligned16(w->w13) || !aligned16(w->w2))
+    return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+// The layer's four stages; when `ev` is given, ev[i] is recorded (as an external
+// event, visible to timing even inside a captured graph) after stage i.
+moe_status forward_stages(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k, int H,
+                          int I, float h_scale, uint16_t* out, void* ws, const moe_forward_layout& L,
+                          cudaStream_t stream, cudaEvent_t* ev, bool external) {
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+  auto mark = [&](int i) -> moe_status {
+    if (!ev) return MOE_OK;
+    cudaError_t e = external ? cudaEventRecordWithFlags(ev[i], stream, cudaEventRecordExternal)
+                             : cudaEventRecord(ev[i], stream);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  };
   const int64_t R = static_cast<int64_t>(T) * k;
   int32_t* topk_id = static_cast<int32_t*>(at(L.topk_id));
   float* topk_w = static_cast<float*>(at(L.topk_w));
@@ -77,27 +96,120 @@ extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const 
   float* hs = static_cast<float*>(at(L.h_scale));
   uint8_t* h_codes = static_cast<uint8_t*>(at(L.h_codes));
   uint8_t* h_sf = static_cast<uint8_t*>(at(L.h_sf));
-
+  moe_status s = mark(0);
+  if (s != MOE_OK) return s;
   s = moe_route_permute(logits, T, E, k, topk_id, topk_w, offs, p2e, e2p, e2r, at(L.route_ws),
                         moe_route_permute_workspace_size(T, E, k), stream);
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || (s = mark(1)) != MOE_OK) return s;
   s = nvfp4_quantize(x, MOE_IN_BF16, T, H, 1, x_scale, 1, R, k, e2r, x_codes, x_sf, MOE_SF_TILED, L.padded_rows,
                      at(L.quant_ws), nvfp4_quantize_workspace_size(1), stream);
-  if (s != MOE_OK) return s;
+  if (s != MOE_OK || (s = mark(2)) != MOE_OK) return s;
   moe_epilogue_args ep{};
   ep.h_scale = h_scale;
   ep.h_scale_out = hs;
   ep.h_codes = h_codes;
   ep.h_sf = h_sf;
-  s = moe_grouped_gemm_nvfp4(x_codes, x_sf, x_scale, w->w13, w->w13_scale, offs, E, L.padded_rows,
-                             2 * I, H, MOE_EPI_SILU_MUL_QUANT, &ep, nullptr, nullptr, 0, stream);
-  if (s != MOE_OK) return s;
+  s = moe_grouped_gemm_nvfp4(x_codes, x_sf, x_scale, w->w13, w->w13_scale, offs, E, L.padded_rows, 2 * I, H,
+                             MOE_EPI_SILU_MUL_QUANT, &ep, nullptr, nullptr, 0, stream);
+  if (s != MOE_OK || (s = mark(3)) != MOE_OK) return s;
   moe_epilogue_args ep2{};
   ep2.perm_to_expanded = p2e;
   ep2.topk_w = topk_w;
   ep2.T = T;
   ep2.k = k;
-  return moe_grouped_gemm_nvfp4(h_codes, h_sf, hs, w->w2, w->w2_scale, offs, E, L.padded_rows, H, I,
-                                MOE_EPI_FINALIZE, &ep2, out, at(L.gemm_ws),
-                                moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H), stream);
+  s = moe_grouped_gemm_nvfp4(h_codes, h_sf, hs, w->w2, w->w2_scale, offs, E, L.padded_rows, H, I, MOE_EPI_FINALIZE,
+                             &ep2, out, at(L.gemm_ws), moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H),
+                             stream);
+  if (s != MOE_OK) return s;
+  return mark(4);
 }
+
+}  // namespace
+
+extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k,
+                                  int H, int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  moe_forward_layout L;
+  moe_status s = forward_check(x, logits, w, T, E, k, H, I, h_scale, out, ws, ws_bytes, &L);
+  if (s != MOE_OK) return s;
+  return forward_stages(x, logits, w, T, E, k, H, I, h_scale, out, ws, L, static_cast<cudaStream_t>(stream), nullptr,
+                        false);
+}
+
+// ---------------------------------------------------------------------------
+// The layer as one CUDA graph: captured once, replayed with one launch.
+// ---------------------------------------------------------------------------
+struct moe_forward_graph {
+  cudaGraphExec_t exec = nullptr;
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool timed = false;
+};
+
+namespace {
+void graph_release(moe_forward_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  for (auto& e : g->ev)
+    if (e) cudaEventDestroy(e);
+  delete g;
+}
+}  // namespace
+
+extern "C" moe_status moe_forward_graph_create(const uint16_t* x, const float* logits, const moe_weights* w, int T,
+                                               int E, int k, int H, int I, float h_scale, uint16_t* out, void* ws,
+                                               size_t ws_bytes, int stage_events, moe_forward_graph** graph) {
+  if (!graph) return MOE_ERR_INVALID_ARG;
+  *graph = nullptr;
+  moe_forward_layout L;
+  moe_status s = forward_check(x, logits, w, T, E, k, H, I, h_scale, out, ws, ws_bytes, &L);
+  if (s != MOE_OK) return s;
+  if (!device_error_word() || num_sms() < 1) return MOE_ERR_CUDA;
+  moe_forward_graph* g = new moe_forward_graph();
+  g->timed = stage_events != 0;
+  cudaStream_t st = nullptr;
+  cudaGraph_t raw = nullptr;
+  auto fail = [&](moe_status code) {
+    if (raw) cudaGraphDestroy(raw);
+    if (st) cudaStreamDestroy(st);
+    graph_release(g);
+    return code;
+  };
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (g->timed)
+    for (auto& e : g->ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  // One eager pass first: every host-side preparation (kernel attributes, cached
+  // device addresses) happens outside the capture.
+  s = forward_stages(x, logits, w, T, E, k, H, I, h_scale, out, ws, L, st, nullptr, false);
+  if (s != MOE_OK) return fail(s);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  s = forward_stages(x, logits, w, T, E, k, H, I, h_scale, out, ws, L, st, g->timed ? g->ev : nullptr, true);
+  cudaError_t ce = cudaStreamEndCapture(st, &raw);
+  if (s != MOE_OK) return fail(s);
+  if (ce != cudaSuccess || !raw) return fail(MOE_ERR_CUDA);
+  if (cudaGraphInstantiate(&g->exec, raw, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  cudaGraphDestroy(raw);
+  raw = nullptr;
+  cudaStreamDestroy(st);
+  st = nullptr;
+  *graph = g;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_forward_graph_launch(moe_forward_graph* graph, void* stream) {
+  if (!graph || !graph->exec) return MOE_ERR_INVALID_ARG;
+  return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status moe_forward_graph_stage_ms(moe_forward_graph* graph, float* ms) {
+  if (!graph || !ms) return MOE_ERR_INVALID_ARG;
+  if (!graph->timed) return MOE_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(graph->ev[4]) != cudaSuccess) return MOE_ERR_CUDA;
+  for (int i = 0; i < 4; ++i)
+    if (cudaEventElapsedTime(&ms[i], graph->ev[i], graph->ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaEventElapsedTime(&ms[4], graph->ev[0], graph->ev[4]) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+extern "C" void moe_forward_graph_destroy(moe_forward_graph* graph) { graph_release(graph); }

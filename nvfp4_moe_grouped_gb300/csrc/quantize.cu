@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, i
   if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(amax_bits + g, __float_as_uint(m));
 }
 
+// Decode multiplier of every group from its amax (used when the quantise kernel
+// does not visit every group's first row).
 __global__ void scale_from_amax_kernel(const uint32_t* __restrict__ amax_bits, int groups, float* __restrict__ scale) {
   int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
@@ -121,14 +123,28 @@ MOE_DEVINL uint32_t quantize_block16(const void* x, int64_t row, int K, int blk,
 // codes and 4 contiguous scale bytes (one aligned word in every layout).
 template <int IN_F32, int LAYOUT>
 __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
-    const void* __restrict__ x, int64_t rows_per_group, int K, const float* __restrict__ scale, int64_t n_src,
-    int fan, const int32_t* __restrict__ dst_row, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
+    const void* __restrict__ x, int64_t rows_per_group, int K, const uint32_t* __restrict__ amax_bits,
+    float* __restrict__ scale, int64_t n_src, int n_slices, int fan, const int32_t* __restrict__ dst_row,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ sf) {
   const int lane = threadIdx.x & 31;
-  const int64_t src = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t w = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t src = w / n_slices;
+  const int slice = static_cast<int>(w - src * n_slices);
   if (src >= n_src) return;
-  const float s = __ldg(scale + src / rows_per_group);
+  const int64_t g = src / rows_per_group;
+  float s;
+  if (amax_bits) {
+    // dynamic scale: s = amax / (6 * 448) of the row's group (1 when the group is all zero); the
+    // first warp of the group publishes it
+    const float a = __uint_as_float(__ldg(amax_bits + g));
+    s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+    if (src == g * rows_per_group && slice == 0 && lane == 0) scale[g] = s;
+  } else {
+    s = __ldg(scale + g);
+  }
   if (K % 64 == 0) {
-    for (int q = lane; q < K / 64; q += 32) {
+    // this warp's slice: quads [32 * slice, 32 * slice + 32), one per lane
+    for (int q = 32 * slice + lane; q < min(K / 64, 32 * slice + 32); q += 32) {
       uint32_t c[8];
       uint32_t sf4 = 0;
 #pragma unroll
@@ -205,6 +221,14 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
   if (src_div > 1 && (src_div > 32 || n_items != src_rows * src_div)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(codes) || (sf && !aligned16(sf))) return MOE_ERR_MISALIGNED;
   if (dynamic_scale && (!ws || ws_bytes < nvfp4_quantize_workspace_size(groups))) return MOE_ERR_WORKSPACE;
+  // Launch geometry first, so a shape the grid cannot express is rejected before anything is enqueued.
+  const bool fan_out = src_div > 1;
+  const int fan = fan_out ? src_div : 1;
+  const int64_t n_src = fan_out ? src_rows : n_items;
+  // rows split into slices of 32 x 64 elements so short batches still fill the GPU
+  const int n_slices = (K % 64 == 0) ? (K / 64 + 31) / 32 : 1;
+  const int64_t blocks = (n_src * n_slices + kQuantWarps - 1) / kQuantWarps;
+  if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t rows_per_group = src_rows / groups;
   if (dynamic_scale) {
@@ -219,20 +243,20 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
       amax_kernel<1><<<grid, 256, 0, st>>>(x, rows_per_group, K, amax);
     else
       amax_kernel<0><<<grid, 256, 0, st>>>(x, rows_per_group, K, amax);
-    scale_from_amax_kernel<<<(groups + 255) / 256, 256, 0, st>>>(amax, groups, tensor_scale);
   }
+  const bool covers_all_rows = (src_div > 1) || (n_items == src_rows);
+  if (dynamic_scale && (n_items == 0 || !covers_all_rows))
+    scale_from_amax_kernel<<<(groups + 255) / 256, 256, 0, st>>>(static_cast<const uint32_t*>(ws), groups,
+                                                                 tensor_scale);
   if (n_items > 0) {
     // Fan out when every source row is read by src_div consecutive items (the
     // routed-row gather); otherwise one item per warp.
-    const bool fan_out = src_div > 1;
-    const int fan = fan_out ? src_div : 1;
-    const int64_t n_src = fan_out ? src_rows : n_items;
-    int64_t blocks = (n_src + kQuantWarps - 1) / kQuantWarps;
-    if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
     const bool f32 = in_dtype == MOE_IN_F32;
 #define MOE_QLAUNCH(F, T)                                                                                     \
   quantize_kernel<F, T><<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, st>>>(                          \
-      x, rows_per_group, K, tensor_scale, n_src, fan, dst_row, codes, sf)
+      x, rows_per_group, K, (dynamic_scale && covers_all_rows) ? static_cast<const uint32_t*>(ws) : nullptr,      \
+      tensor_scale, n_src, n_slices,                                                                           \
+      fan, dst_row, codes, sf)
     if (f32) {
       if (sf_layout == MOE_SF_BLOCKED) MOE_QLAUNCH(1, 2);
       else if (sf_layout == MOE_SF_TILED) MOE_QLAUNCH(1, 1);

@@ -384,3 +384,40 @@ def test_timeout_path_reports_and_recovers():
     xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
     ref = oracle.grouped_gemm(xc, xs, xsc, *oracle.quantize_weights(w.numpy()), offs, N, K)
     tol_check(bf16_to_np(out)[dst], ref, "after timeout")
+
+
+def test_forward_graph_replays_the_layer():
+    """moe_forward captured as one CUDA graph: the replay matches the oracle, and refilling the
+    inputs in place then relaunching matches an eager moe_forward on the new inputs."""
+    T, E, k, H, I = 16, 8, 2, 256, 128
+    x, logits, w13f, w2f = _layer_case(T, E, k, H, I)
+    w13 = oracle.quantize_weights(w13f.numpy())
+    w2 = oracle.quantize_weights(w2f.numpy())
+    ref = oracle.moe_layer(x.float().numpy(), logits.numpy(), w13, w2, k)
+    h_scale = float(oracle.tensor_scale_from_amax(oracle.amax(ref.h.astype(np.float32))))
+    pw13 = moe.prepare_expert_weights(w13f.to(DEV), gate_up=True)
+    pw2 = moe.prepare_expert_weights(w2f.to(DEV), gate_up=False)
+    fwd = moe.MoeForward(T, E, k, H, I)
+    xd, ld = x.to(DEV), logits.to(DEV)
+    g = fwd.graph(xd, ld, pw13, pw2, h_scale, stage_events=True)
+    out = g.launch()
+    torch.cuda.synchronize()
+    got = bf16_to_np(out)
+    assert np.linalg.norm(got - ref.out) / np.linalg.norm(ref.out) < 1e-2
+    ms = g.stage_ms()
+    assert all(m > 0 for m in ms) and abs(sum(ms[:4]) - ms[4]) < 1e-3 * max(1.0, ms[4]) + 1e-3
+    # new inputs, same buffers
+    x2 = inputs.activations(T, H, seed=123)
+    l2 = inputs.router_logits(T, E, seed=456)
+    xd.copy_(x2.to(DEV))
+    ld.copy_(l2.to(DEV))
+    out = g.launch()
+    torch.cuda.synchronize()
+    eager = moe.moe_forward(x2.to(DEV), l2.to(DEV), pw13, pw2, k, h_scale)
+    torch.cuda.synchronize()
+    ref2 = oracle.moe_layer(x2.float().numpy(), l2.numpy(), w13, w2, k, h_scale=h_scale)
+    a, b = bf16_to_np(out), bf16_to_np(eager)
+    assert np.linalg.norm(a - ref2.out) / np.linalg.norm(ref2.out) < 1e-2
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-3
+    g.close()
+    assert moe.device_error() == (0, 0)
