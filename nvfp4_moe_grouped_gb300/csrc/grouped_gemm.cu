@@ -37,8 +37,9 @@
 //     tcgen05.mma instructions and their commits, warps 2-5 drain the
 //     accumulator (tcgen05.ld) and run the epilogue.  A tcgen05.cp of the
 //     scales on the MMA thread would serialise with the MMA that reads them:
-//     at decode that halved the weight-streaming rate.  Two TMEM accumulators
-//     let the epilogue of one unit overlap the mainloop of the next; every
+//     at decode that halved the weight-streaming rate.  Several TMEM
+//     accumulators (four for the 64-row tile, two for the 128-row one) let the
+//     epilogue of one unit overlap the mainloops of the next ones; every
 //     stage has its own TMEM scale slot, recycled by the same commit that
 //     frees the stage.
 //   * Every wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT in the
@@ -74,7 +75,10 @@ struct Cfg {
   static constexpr int kStages = BN == 64 ? 7 : 5;
   static constexpr int kXStageBytes = BN * kBK / 2;
   static constexpr uint32_t kAccCols = BN;
-  static constexpr uint32_t kSfTmemBase = 2 * BN;
+  // Accumulator buffers: the epilogue of a unit may lag the mainloop by kAccBufs - 1 units
+  // (decode units are short, so the 64-row tile keeps four).
+  static constexpr int kAccBufs = BN == 64 ? 4 : 2;
+  static constexpr uint32_t kSfTmemBase = kAccBufs * BN;
   static_assert(kSfTmemBase + kStages * kSfSlotCols <= kTmemCols, "tensor memory budget");
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int w = 0;
@@ -83,8 +87,8 @@ struct Cfg {
   static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][kEpiStride]
   static constexpr int tok_t = epi + 32 * kEpiStride * 4;    // int [BN]
   static constexpr int tok_w = tok_t + BN * 4;               // float [BN]
-  static constexpr int bars = tok_w + BN * 4;                // uint64 [3*kStages + 5]
-  static constexpr int misc = bars + (3 * kStages + 5) * 8;  // tmem base, abort flag
+  static constexpr int bars = tok_w + BN * 4;                // uint64 [3*kStages + 2*kAccBufs + 1]
+  static constexpr int misc = bars + (3 * kStages + 2 * kAccBufs + 1) * 8;  // tmem base, abort flag
   static constexpr int sched = misc + 16;                    // int [3][kMaxExperts+1]
   static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
   static constexpr int smem_bytes = total + 1024;            // + alignment slack
@@ -168,7 +172,8 @@ MOE_DEVINL bool epi_any(bool pred) {
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const GemmParams p) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xt,
+                        const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -183,8 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + S;
   uint64_t* sf_ready = empty + S;
   uint64_t* acc_full = sf_ready + S;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* mma_done = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + C::kAccBufs;
+  uint64_t* mma_done = acc_empty + C::kAccBufs;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::misc + 4);
   int* unit_start = reinterpret_cast<int*>(smem + C::sched);
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- prologue: barriers, tensor memory, work list --------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sf_ready[s], 4); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
+    for (int b = 0; b < C::kAccBufs; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
     mbar_init(mma_done, 1);
     *s_abort = 0;
     fence_barrier_init();
@@ -276,9 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&full[stage], bytes);
             bulk_load(s_w + stage * kWStageBytes, w_src + static_cast<int64_t>(kt) * kWStageBytes, kWStageBytes,
                       &full[stage], pol_w);
-            for (int q = 0; q < d.n_mma / 32; ++q)
-              tma_load_2d(s_x + stage * C::kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage], kt * (kBK / 2),
-                          d.x_row + 32 * q, pol_x);
+            if (d.n_mma == BN) {
+              // a full tile: one box of BN rows (tm_xt)
+              tma_load_2d(s_x + stage * C::kXStageBytes, &tm_xt, &full[stage], kt * (kBK / 2), d.x_row, pol_x);
+            } else {
+              for (int q = 0; q < d.n_mma / 32; ++q)
+                tma_load_2d(s_x + stage * C::kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage],
+                            kt * (kBK / 2), d.x_row + 32 * q, pol_x);
+            }
             bulk_load(s_sfx + stage * kSfStageBytes, sfx_src + kt * 4 * 512, steps * 512, &full[stage], pol_x);
             issued[stage] += 1;
           }
@@ -302,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++acc_i) {
         const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
         if (!d.valid) { --acc_i; continue; }
-        const int b = acc_i & 1;
-        if (!mbar_wait_bounded(&acc_empty[b], ((acc_i >> 1) & 1) ^ 1u, p.timeout_ns, s_abort)) {
+        const int b = acc_i % C::kAccBufs;
+        if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
           if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 2);
           *s_abort = 1;
           break;
@@ -402,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         --acc_i;
         continue;
       }
-      const int b = acc_i & 1;
-      const bool got = mbar_wait_bounded(&acc_full[b], (acc_i >> 1) & 1, p.timeout_ns, s_abort);
+      const int b = acc_i % C::kAccBufs;
+      const bool got = mbar_wait_bounded(&acc_full[b], (acc_i / C::kAccBufs) & 1, p.timeout_ns, s_abort);
       // The four epilogue warps decide together, so none is left waiting on a
       // named barrier that the others have abandoned.
       if (epi_any(!got)) {
@@ -556,15 +566,21 @@ bool make_code_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t ro
 }
 
 template <int BN>
-moe_status launch_gemm(const CUtensorMap& tm_x, const GemmParams& p, int64_t max_units, cudaStream_t st) {
+moe_status prepare_gemm() {
+  return cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<BN>::smem_bytes) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_RESOURCE;
+}
+
+template <int BN>
+moe_status launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_xt, const GemmParams& p, int64_t max_units,
+                       cudaStream_t st) {
   using C = Cfg<BN>;
-  if (cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem_bytes) !=
-      cudaSuccess)
-    return MOE_ERR_RESOURCE;
   int grid = num_sms();
   if (grid < 1) return MOE_ERR_CUDA;
   if (max_units < grid) grid = static_cast<int>(max_units);
-  grouped_gemm_kernel<BN><<<grid, kThreads, C::smem_bytes, st>>>(tm_x, p);
+  grouped_gemm_kernel<BN><<<grid, kThreads, C::smem_bytes, st>>>(tm_x, tm_xt, p);
   return check_launch();
 }
 
@@ -649,16 +665,22 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   p.debug_flags = gemm_debug_flags();
   if (!p.err) return MOE_ERR_CUDA;
 
-  CUtensorMap tm_x;
+  const int bn = gemm_tile_rows(a_rows_alloc, E);
+  // routed-row tiles come as 32-row boxes, or as one box when a unit fills the whole tile
+  CUtensorMap tm_x, tm_xt;
   if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
+  if (!make_code_map(&tm_xt, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, bn)) return MOE_ERR_CUDA;
+  {
+    const moe_status ps = bn == 64 ? prepare_gemm<64>() : prepare_gemm<128>();
+    if (ps != MOE_OK) return ps;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (epilogue == MOE_EPI_FINALIZE && !p.fin_gather) {
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  const int bn = gemm_tile_rows(a_rows_alloc, E);
   const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
-  moe_status s = bn == 64 ? launch_gemm<64>(tm_x, p, max_units, st) : launch_gemm<128>(tm_x, p, max_units, st);
+  moe_status s = bn == 64 ? launch_gemm<64>(tm_x, tm_xt, p, max_units, st) : launch_gemm<128>(tm_x, tm_xt, p, max_units, st);
   if (s != MOE_OK) return s;
   if (epilogue == MOE_EPI_FINALIZE) {
     if (p.fin_gather)

@@ -20,7 +20,8 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 256;      // scatter: one thread per (token, slot) item of a chunk
+constexpr int kTopkThreads = 1024;      // top-k: one warp per token of a chunk
 
 struct RouteDims {
   int T, E, k, chunk_tokens, n_chunks;
@@ -39,7 +40,7 @@ inline RouteDims route_dims(int T, int E, int k) {
 MOE_DEVINL bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 template <int NV>  // logits per lane: NV * 32 >= E
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, RouteDims d,
+__global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __restrict__ logits, RouteDims d,
                                                               int32_t* __restrict__ topk_id,
                                                               float* __restrict__ topk_w,
                                                               int32_t* __restrict__ chunk_counts) {
@@ -50,7 +51,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
 
-  for (int t = t0 + warp; t < t1; t += kRouteThreads / 32) {
+  for (int t = t0 + warp; t < t1; t += kTopkThreads / 32) {
     const float* row = logits + static_cast<int64_t>(t) * d.E;
     float v[NV];
     uint32_t taken = 0;
@@ -222,7 +223,7 @@ extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k
   int32_t* pads = route_pad_offsets(ws, T, E, k);
   const size_t hist_bytes = sizeof(int) * E;
   const int nv = (E + 31) / 32;
-#define MOE_ROUTE(NV) route_kernel<NV><<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts)
+#define MOE_ROUTE(NV) route_kernel<NV><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts)
   if (nv <= 1) MOE_ROUTE(1);
   else if (nv <= 2) MOE_ROUTE(2);
   else if (nv <= 4) MOE_ROUTE(4);
