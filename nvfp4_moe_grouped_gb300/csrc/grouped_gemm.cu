@@ -29,9 +29,11 @@
 //     exact shared-memory image the MMA descriptor reads) and its four scale
 //     atoms, so each pipeline stage of weights is ONE linear bulk copy that
 //     streams a contiguous 18 KB run of HBM.
-//   * Warp roles: warp 0 issues the copies (weights: bulk copy, evict-first;
-//     routed rows: 2D tensor-map loads of 32 rows with 128-byte swizzle and
-//     a bulk copy of their scale atoms, evict-last), warps 6-9 move each
+//   * Warp roles: warps 0 and 10-12 issue the copies, each one stage fill in
+//     four (weights: bulk copy, evict-first; routed rows: 2D tensor-map loads
+//     with 128-byte swizzle and a bulk copy of their scale atoms, evict-last);
+//     one issuing thread gets its bulk copies served one after another, which
+//     caps a single producer near 5 TB/s of L2 hits per GPU.  Warps 6-9 move each
 //     stage's scale atoms from shared into tensor memory (tcgen05.st, one
 //     warp per lane quadrant), warp 1 owns tensor memory and issues only the
 //     tcgen05.mma instructions and their commits, warps 2-5 drain the
@@ -64,7 +66,9 @@ constexpr int kBM = 128;                  // weight rows per tile (MMA M)
 constexpr int kBK = 256;                  // K elements per stage (128 bytes per row)
 constexpr int kWStageBytes = kBlockedTileBytes;  // 16 KB codes + 2 KB scale atoms
 constexpr int kSfStageBytes = 4 * 512;    // scale atoms of the routed rows (one per 64-element K step)
-constexpr int kThreads = 320;  // warp 0 copies, 1 MMA, 2-5 epilogue, 6-9 scale staging
+constexpr int kProducers = 4;            // copy-issuing warps: 0 and 10 .. 8 + kProducers
+constexpr int kFirstExtraProducer = 10;
+constexpr int kThreads = 32 * (kFirstExtraProducer + kProducers - 1);  // 1 MMA, 2-5 epilogue, 6-9 scale staging
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfSlotCols = 32;      // 16 columns weight scales + 16 columns routed-row scales
@@ -80,6 +84,11 @@ struct Cfg {
   static constexpr int kAccBufs = BN == 64 ? 4 : 2;
   static constexpr uint32_t kSfTmemBase = kAccBufs * BN;
   static_assert(kSfTmemBase + kStages * kSfSlotCols <= kTmemCols, "tensor memory budget");
+  // A producer waits on a stage's `empty` barrier by phase parity, so that barrier
+  // must never be two phases behind the fill being waited for.  The producer's
+  // previous fill (kProducers back) could only start once fill - kProducers - kStages
+  // had been consumed; with kProducers <= kStages that covers fill - 2 * kStages.
+  static_assert(kStages >= kProducers, "more producers than stages would alias barrier phases");
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int w = 0;
   static constexpr int x = w + kStages * kWStageBytes;
@@ -89,7 +98,8 @@ struct Cfg {
   static constexpr int tok_w = tok_t + BN * 4;               // float [BN]
   static constexpr int bars = tok_w + BN * 4;                // uint64 [3*kStages + 2*kAccBufs + 1]
   static constexpr int misc = bars + (3 * kStages + 2 * kAccBufs + 1) * 8;  // tmem base, abort flag
-  static constexpr int sched = misc + 16;                    // int [3][kMaxExperts+1]
+  static constexpr int last = misc + 16;                     // int [kProducers][kStages]
+  static constexpr int sched = last + kProducers * kStages * 4;  // int [3][kMaxExperts+1]
   static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
   static constexpr int smem_bytes = total + 1024;            // + alignment slack
   static_assert(smem_bytes <= 232448, "shared memory budget");
@@ -126,10 +136,20 @@ struct Unit {
   bool valid;  // false when the offsets place the unit outside the routed-row allocation
 };
 
-MOE_DEVINL int find_expert(const int* start, int E, int u) {
-  int lo = 0, hi = E;  // start[lo] <= u < start[hi]
+// The expert owning unit u (start[e] <= u < start[e + 1]), searched from `e`, an
+// expert at or before the owner: every role walks its units in increasing order,
+// so the search gallops forward from the previous owner instead of bisecting all
+// E experts (shared-memory loads are slow on the MMA-issuing thread).
+MOE_DEVINL int find_expert_from(const int* start, int E, int u, int e) {
+  int lo = e, step = 1, hi = e + 1;
+  while (hi < E && start[hi] <= u) {
+    lo = hi;
+    step <<= 1;
+    hi = lo + step;
+  }
+  if (hi > E) hi = E;  // start[E] = total units > u
   while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
+    const int mid = (lo + hi) >> 1;
     if (start[mid] <= u) lo = mid; else hi = mid;
   }
   return lo;
@@ -137,9 +157,9 @@ MOE_DEVINL int find_expert(const int* start, int E, int u) {
 
 template <int BN>
 MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MT,
-                            int64_t rows_alloc) {
+                            int64_t rows_alloc, int& e_hint) {
   Unit d;
-  d.e = find_expert(unit_start, E, u);
+  d.e = e_hint = find_expert_from(unit_start, E, u, e_hint);
   const int local = u - unit_start[d.e];
   d.nb = local / MT;
   d.mt = local - d.nb * MT;
@@ -250,57 +270,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *s_tmem;
   const int total_units = unit_start[E];
 
-  if (warp == 0) {
-    // ---------------- producer ----------------
+  if (warp == 0 || warp >= kFirstExtraProducer) {
+    // ---------------- producers ----------------
+    // Stage fill i (counted over this CTA's units and K steps) is issued by
+    // producer i % kProducers: bulk copies from one issuing thread are served
+    // one after another, so several issuing warps keep more of them in flight
+    // (the weight and token tiles of a compute-bound unit are mostly L2 hits).
+    const int pid = warp == 0 ? 0 : warp - kFirstExtraProducer + 1;
+    int* s_last = reinterpret_cast<int*>(smem + C::last);  // [kProducers][S] last fill index per stage
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      int issued[S];
-      for (int s = 0; s < S; ++s) issued[s] = 0;
-      bool skip_once = (p.debug_flags & 1) != 0;
+      int fill = 0;
+      for (int s = 0; s < S; ++s) s_last[pid * S + s] = -1;
+      bool skip_once = pid == 0 && (p.debug_flags & 1) != 0;
+      int e_hint = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
         if (!d.valid) continue;
         const uint8_t* w_src = p.w_blocked + static_cast<int64_t>(d.e * MT + d.mt) * KT * kWStageBytes;
         const uint8_t* sfx_src = p.x_sf + static_cast<int64_t>(d.x_row / 128) * (K / 64) * 512;
-        for (int kt = 0; kt < KT; ++kt) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, s_abort)) {
-            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 1);
-            *s_abort = 1;
-            ok = false;
-            break;
-          }
-          const int steps = min(4, (K - kt * kBK) / 64);
-          if (skip_once) {
-            skip_once = false;  // test hook: this stage is never filled
-          } else {
-            const uint32_t bytes = kWStageBytes + d.n_mma * (kBK / 2) + steps * 512;
-            mbar_arrive_expect_tx(&full[stage], bytes);
-            bulk_load(s_w + stage * kWStageBytes, w_src + static_cast<int64_t>(kt) * kWStageBytes, kWStageBytes,
-                      &full[stage], pol_w);
-            if (d.n_mma == BN) {
-              // a full tile: one box of BN rows (tm_xt)
-              tma_load_2d(s_x + stage * C::kXStageBytes, &tm_xt, &full[stage], kt * (kBK / 2), d.x_row, pol_x);
-            } else {
-              for (int q = 0; q < d.n_mma / 32; ++q)
-                tma_load_2d(s_x + stage * C::kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage],
-                            kt * (kBK / 2), d.x_row + 32 * q, pol_x);
+        for (int kt = 0; kt < KT; ++kt, ++fill) {
+          if (fill % kProducers == pid) {
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, s_abort)) {
+              if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 1);
+              *s_abort = 1;
+              ok = false;
+              break;
             }
-            bulk_load(s_sfx + stage * kSfStageBytes, sfx_src + kt * 4 * 512, steps * 512, &full[stage], pol_x);
-            issued[stage] += 1;
+            const int steps = min(4, (K - kt * kBK) / 64);
+            if (skip_once) {
+              skip_once = false;  // test hook: this stage is never filled
+            } else {
+              const uint32_t bytes = kWStageBytes + d.n_mma * (kBK / 2) + steps * 512;
+              mbar_arrive_expect_tx(&full[stage], bytes);
+              bulk_load(s_w + stage * kWStageBytes, w_src + static_cast<int64_t>(kt) * kWStageBytes, kWStageBytes,
+                        &full[stage], pol_w);
+              if (d.n_mma == BN) {
+                // a full tile: one box of BN rows (tm_xt)
+                tma_load_2d(s_x + stage * C::kXStageBytes, &tm_xt, &full[stage], kt * (kBK / 2), d.x_row, pol_x);
+              } else {
+                for (int q = 0; q < d.n_mma / 32; ++q)
+                  tma_load_2d(s_x + stage * C::kXStageBytes + q * 32 * (kBK / 2), &tm_x, &full[stage],
+                              kt * (kBK / 2), d.x_row + 32 * q, pol_x);
+              }
+              bulk_load(s_sfx + stage * kSfStageBytes, sfx_src + kt * 4 * 512, steps * 512, &full[stage], pol_x);
+              s_last[pid * S + stage] = fill;
+            }
           }
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
-      // Let every copy this CTA started land before the CTA can exit.
+    }
+    // Let every copy this CTA started land before the CTA can exit: once all
+    // producers are past their loops, wait for the last fill of every stage
+    // (an earlier fill of a stage has landed before a later one can start).
+    __syncwarp();
+    asm volatile("bar.sync 2, %0;" ::"r"(kProducers * 32) : "memory");
+    if (pid == 0 && lane == 0) {
       int zero = 0;
-      for (int s = 0; s < S; ++s)
-        if (issued[s] > 0)
-          mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued[s] - 1) & 1u, p.timeout_ns,
+      for (int s = 0; s < S; ++s) {
+        int last = -1;
+        for (int q = 0; q < kProducers; ++q) last = max(last, s_last[q * S + s]);
+        if (last >= 0)
+          mbar_wait_bounded(&full[s], static_cast<uint32_t>(last / S) & 1u, p.timeout_ns,
                             reinterpret_cast<volatile int*>(&zero));
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -308,9 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc_i = 0;
+      int e_hint = 0;
       bool ok = true;
+      // Every instruction on this thread delays the next MMA issue, and at a
+      // 128-row tile the tensor core finishes an MMA about as fast as one is
+      // issued: descriptors are precomputed, the four MMAs of a stage unrolled,
+      // and one barrier wait covers two stages (the staging warps complete the
+      // stages in order, so the later stage being ready implies the earlier).
+      const uint64_t adesc0 = smem_desc(smem_u32(s_w), 16, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(smem_u32(s_x), 16, 1024, 2);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++acc_i) {
-        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
         if (!d.valid) { --acc_i; continue; }
         const int b = acc_i % C::kAccBufs;
         if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
@@ -325,23 +371,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (x_row % 128) / 32 TMEM columns into each atom's four columns.
         const uint32_t sfx_col_off = static_cast<uint32_t>((d.x_row & 127) >> 5);
         for (int kt = 0; kt < KT; ++kt) {
-          // sf_ready implies full: the staging warps saw the stage's copies land.
-          if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
-            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 3);
-            *s_abort = 1;
-            ok = false;
-            break;
+          if ((kt & 1) == 0) {
+            // sf_ready implies full: the staging warps saw the stage's copies land.
+            int ws = stage;
+            uint32_t wph = phase;
+            if (kt + 1 < KT && ++ws == S) { ws = 0; wph ^= 1u; }
+            if (!mbar_wait_bounded(&sf_ready[ws], wph, p.timeout_ns, s_abort)) {
+              if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 3);
+              *s_abort = 1;
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
-          const int steps = min(4, (K - kt * kBK) / 64);
           const uint32_t sf_col = tmem_base + C::kSfTmemBase + stage * kSfSlotCols;
-          const uint32_t w_addr = smem_u32(s_w + stage * kWStageBytes);
-          const uint32_t x_addr = smem_u32(s_x + stage * C::kXStageBytes);
-          for (int g = 0; g < steps; ++g) {
-            const uint64_t adesc = smem_desc(w_addr + 32 * g, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(x_addr + 32 * g, 16, 1024, 2);
-            mma_mxf4nvf4(d_tmem, adesc, bdesc, idesc, sf_col + 4 * g, sf_col + 16 + 4 * g + sfx_col_off,
-                         (kt | g) != 0);
+          // start-address field of the descriptors: byte address / 16
+          const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * kWStageBytes) >> 4);
+          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * C::kXStageBytes) >> 4);
+          if (kt * kBK + kBK <= K) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              mma_mxf4nvf4(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g,
+                           sf_col + 16 + 4 * g + sfx_col_off, (kt | g) != 0);
+          } else {
+            const int steps = (K - kt * kBK) / 64;
+            for (int g = 0; g < steps; ++g)
+              mma_mxf4nvf4(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g,
+                           sf_col + 16 + 4 * g + sfx_col_off, (kt | g) != 0);
           }
           mma_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -365,9 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quad_lane = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     int stage = 0;
     uint32_t phase = 0;
+    int e_hint = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
       if (!d.valid) continue;
       for (int kt = 0; kt < KT; ++kt) {
         const bool got = mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort);
@@ -405,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float x_scale = __ldg(p.x_scale);
     if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && et == 0) *p.h_scale_out = p.h_scale;
     int acc_i = 0;
+    int e_hint = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
-      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
       if (!d.valid) {
         if (et == 0) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
         --acc_i;
