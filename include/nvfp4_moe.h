@@ -232,10 +232,13 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  *     `out` is unused.
  *   MOE_EPI_FINALIZE (down): out = bf16 [ep->T][N],
  *     out[t][n] = sum_j topk_w[t][j] * Y[row of item t*k+j][n], summed in FP32
- *     and rounded once.  While T*N*4 bytes <= 64 MiB (an accumulator that
- *     stays in L2) the sum is FP32 atomics in the epilogue (the order of the k
- *     terms is not fixed); above that the epilogue stores each item's weighted
- *     row and a second kernel sums the k rows in slot order.
+ *     and rounded once.  The sum is FP32 atomics in the epilogue (the order
+ *     of the k terms is not fixed) into a T*N*4-byte workspace; when that
+ *     exceeds 64 MiB the kernel takes the weight tiles in column chunks of
+ *     at most 64 MiB of accumulator, so the atomics stay in L2.  Only when one
+ *     128-column chunk is already larger (T > 131072) does the epilogue store
+ *     each item's weighted row (k*T*N*4 bytes) and a second kernel sum the k
+ *     rows in slot order.
  * Arguments:
  *   a_codes/a_sf  activations, padded-row layout, tiled scales, a_rows_alloc rows
  *   a_scale       f32 [1] decode multiplier of A

@@ -23,7 +23,9 @@
 //   * Work unit = (expert, BN-row block of its routed rows, 128-row weight
 //     tile), full K.  Units are ordered expert-major so the CTAs running
 //     together share each expert's token tile in L2.  CTA c takes units c,
-//     c + grid, ...
+//     c + grid, ...  A FINALIZE launch whose FP32 accumulator would not fit
+//     in L2 walks the weight tiles in column chunks (every expert's units of
+//     one chunk, then the next), so its atomics keep hitting L2.
 //   * Weights are prepared in a blocked layout: per 128 rows x 256 K-elements
 //     one contiguous 18 KB block holding the 128-byte-swizzled code tile (the
 //     exact shared-memory image the MMA descriptor reads) and its four scale
@@ -53,12 +55,22 @@ namespace moe {
 moe_status launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t st);
 moe_status launch_finalize_sum(const float* rows, int T, int k, int N, uint16_t* out, cudaStream_t st);
 
-// FINALIZE accumulates with atomics into a [T][N] FP32 buffer while that buffer
-// fits comfortably in L2; above this size every atomic would miss to HBM, so the
-// epilogue instead stores each expanded item's weighted row and a second kernel
-// sums the k rows of every token (deterministically, in slot order).
+// FINALIZE accumulates with atomics into a [T][N] FP32 buffer.  The atomics stay
+// in L2 while the part of that buffer being written fits comfortably there: the
+// kernel walks the weight tiles in column chunks of `mt_chunk` 128-row tiles (all
+// experts' units of one chunk before the next chunk), so the live part is
+// T x 128*mt_chunk floats.  Returns the largest chunk (a divisor of N/128) whose
+// live part is at most kFinalizeAtomicMaxBytes, or 0 when not even one tile
+// column fits; the epilogue then stores each expanded item's weighted row and a
+// second kernel sums the k rows of every token (deterministically, in slot order).
 constexpr int64_t kFinalizeAtomicMaxBytes = 64ll << 20;
-inline bool finalize_gathers(int T, int N) { return static_cast<int64_t>(T) * N * 4 > kFinalizeAtomicMaxBytes; }
+inline int finalize_mt_chunk(int T, int N) {
+  const int MT = N / 128;
+  for (int c = MT; c >= 1; --c)
+    if (MT % c == 0 && static_cast<int64_t>(T) * c * 128 * 4 <= kFinalizeAtomicMaxBytes) return c;
+  return 0;
+}
+inline bool finalize_gathers(int T, int N) { return finalize_mt_chunk(T, N) == 0; }
 
 namespace {
 
@@ -125,6 +137,7 @@ struct GemmParams {
   int k;
   int T;
   int fin_gather;             // FINALIZE: 1 = store weighted rows per expanded item (summed later), 0 = atomics
+  int mt_chunk;               // weight tiles per column chunk of the unit order (N/128 = one chunk)
   int64_t rows_alloc;         // rows of the routed-row operand (bounds every access to it)
   int32_t* err;
   uint64_t timeout_ns;
@@ -155,14 +168,20 @@ MOE_DEVINL int find_expert_from(const int* start, int E, int u, int e) {
   return lo;
 }
 
+// Unit u -> (column chunk c, expert e, routed-row block nb, weight tile mt):
+// U units per chunk, ordered expert-major, each routed-row block taking MTC
+// consecutive units (the chunk's weight tiles).
 template <int BN>
-MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MT,
+MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MTC, int U,
                             int64_t rows_alloc, int& e_hint) {
   Unit d;
-  d.e = e_hint = find_expert_from(unit_start, E, u, e_hint);
-  const int local = u - unit_start[d.e];
-  d.nb = local / MT;
-  d.mt = local - d.nb * MT;
+  const int c = u / U;
+  const int uc = u - c * U;
+  if (unit_start[e_hint] > uc) e_hint = 0;  // a new column chunk starts over at expert 0
+  d.e = e_hint = find_expert_from(unit_start, E, uc, e_hint);
+  const int local = uc - unit_start[d.e];
+  d.nb = local / MTC;
+  d.mt = c * MTC + (local - d.nb * MTC);
   const int m_e = off[d.e + 1] - off[d.e];
   d.rows = min(BN, m_e - d.nb * BN);
   d.n_mma = d.rows <= 32 ? 32 : (d.rows <= 64 ? 64 : 128);
@@ -219,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, N = p.N, K = p.K;
   const int MT = N / kBM;
+  const int MTC = p.mt_chunk;
   const int KT = (K + kBK - 1) / kBK;
 
   // ---- prologue: barriers, tensor memory, work list --------------------
@@ -240,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int units = 0, pads = 0;
     for (int e = e0; e < min(E, e0 + per); ++e) {
       const int m = __ldg(p.expert_offsets + e + 1) - __ldg(p.expert_offsets + e);
-      units += ((m + BN - 1) / BN) * MT;
+      units += ((m + BN - 1) / BN) * MTC;
       pads += ((m + 127) / 128) * 128;
     }
     int iu = units, ip = pads;
@@ -255,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unit_start[e] = ru;
       pad_start[e] = rp;
       off[e] = o0;
-      ru += ((o1 - o0 + BN - 1) / BN) * MT;
+      ru += ((o1 - o0 + BN - 1) / BN) * MTC;
       rp += ((o1 - o0 + 127) / 128) * 128;
     }
     if (lane == 31) {
@@ -268,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const int total_units = unit_start[E];
+  const int U = unit_start[E];
+  const int total_units = U * (MT / MTC);
 
   if (warp == 0 || warp >= kFirstExtraProducer) {
     // ---------------- producers ----------------
@@ -289,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int e_hint = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
         if (!d.valid) continue;
         const uint8_t* w_src = p.w_blocked + static_cast<int64_t>(d.e * MT + d.mt) * KT * kWStageBytes;
         const uint8_t* sfx_src = p.x_sf + static_cast<int64_t>(d.x_row / 128) * (K / 64) * 512;
@@ -356,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t adesc0 = smem_desc(smem_u32(s_w), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(s_x), 16, 1024, 2);
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++acc_i) {
-        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
         if (!d.valid) { --acc_i; continue; }
         const int b = acc_i % C::kAccBufs;
         if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
@@ -424,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int e_hint = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
       if (!d.valid) continue;
       for (int kt = 0; kt < KT; ++kt) {
         const bool got = mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort);
@@ -464,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc_i = 0;
     int e_hint = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
-      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MT, p.rows_alloc, e_hint);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
       if (!d.valid) {
         if (et == 0) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
         --acc_i;
@@ -716,7 +737,9 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
     p.k = ep->k;
     p.T = ep->T;
     p.fin_gather = finalize_gathers(ep->T, N) ? 1 : 0;
+    if (!p.fin_gather) p.mt_chunk = finalize_mt_chunk(ep->T, N);
   }
+  if (p.mt_chunk == 0) p.mt_chunk = N / kBM;
   p.rows_alloc = a_rows_alloc;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
@@ -724,6 +747,8 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   if (!p.err) return MOE_ERR_CUDA;
 
   const int bn = gemm_tile_rows(a_rows_alloc, E);
+  const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
+  if (max_units > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   // routed-row tiles come as 32-row boxes, or as one box when a unit fills the whole tile
   CUtensorMap tm_x, tm_xt;
   if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
@@ -737,7 +762,6 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
   moe_status s = bn == 64 ? launch_gemm<64>(tm_x, tm_xt, p, max_units, st) : launch_gemm<128>(tm_x, tm_xt, p, max_units, st);
   if (s != MOE_OK) return s;
   if (epilogue == MOE_EPI_FINALIZE) {

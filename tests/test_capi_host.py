@@ -74,7 +74,10 @@ def test_blocked_weight_bytes(L):
 def test_workspace_queries(L):
     assert L.moe_grouped_gemm_workspace_size(moe.EPI_NONE, 1024, 8, 6144) == 0
     assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 1024, 8, 6144) == 1024 * 6144 * 4      # atomics
-    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 16384, 8, 6144) == 16384 * 8 * 6144 * 4  # rows
+    # past 64 MiB the atomics take column chunks; per-item rows only when one 128-column chunk is too large
+    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 16384, 8, 6144) == 16384 * 6144 * 4
+    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 131072, 8, 6144) == 131072 * 6144 * 4
+    assert L.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, 131073, 2, 256) == 131073 * 2 * 256 * 4
     assert L.nvfp4_quantize_workspace_size(1) == 256
     assert L.moe_route_permute_workspace_size(1024, 256, 8) >= (1024 // 32) * 256 * 4
 

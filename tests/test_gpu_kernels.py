@@ -310,6 +310,30 @@ def test_grouped_gemm_finalize_matches_oracle(T, E, k, H, I):
     tol_check(bf16_to_np(out), ref, "FINALIZE")
 
 
+@pytest.mark.parametrize("T,E,k,H,I,mode", [(20000, 4, 2, 1024, 64, "chunked"), (132000, 2, 1, 128, 64, "rows")])
+def test_grouped_gemm_finalize_large_T_modes(T, E, k, H, I, mode):
+    """FINALIZE past an L2-sized accumulator: column-chunked atomics, and per-item rows summed in slot order."""
+    ws = moe._lib.load().moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, T, k, H)
+    assert ws == (T * H * 4 if mode == "chunked" else T * k * H * 4)
+    logits = inputs.router_logits(T, E, seed=7).numpy()
+    ids, w = oracle.route(logits, k)
+    offs, p2e, e2p = oracle.permute(ids, E)
+    g = torch.Generator().manual_seed(11)
+    h = (torch.randn(T * k, I, generator=g) * 0.3).numpy()
+    hc, hs, hsc = oracle.quantize_dynamic(h)
+    w2 = inputs.expert_weights(E, H, I, 600)
+    w2q = oracle.quantize_weights(w2.numpy())
+    ref = oracle.finalize(oracle.grouped_gemm(hc, hs, hsc, *w2q, offs, H, I), w, e2p)
+    codes, sf, s, dst = _routed_operand(torch.from_numpy(h), offs.astype(np.int64))
+    pw = moe.prepare_expert_weights(w2.to(DEV), gate_up=False)
+    out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV), moe.EPI_FINALIZE,
+                                     perm_to_expanded=torch.from_numpy(p2e).to(DEV),
+                                     topk_w=torch.from_numpy(w).to(DEV), T=T, k=k)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    tol_check(bf16_to_np(out), ref, "FINALIZE " + mode)
+
+
 # ------------------------------------------------------------------ fused layer
 
 def _layer_case(T, E, k, H, I, zipf=None):
