@@ -106,9 +106,9 @@ struct Cfg {
   static constexpr int x = w + kStages * kWStageBytes;
   static constexpr int sfx = x + kStages * kXStageBytes;
   static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][kEpiStride]
-  static constexpr int tok_t = epi + 32 * kEpiStride * 4;    // int [BN]
-  static constexpr int tok_w = tok_t + BN * 4;               // float [BN]
-  static constexpr int bars = tok_w + BN * 4;                // uint64 [3*kStages + 2*kAccBufs + 1]
+  static constexpr int tok_t = epi + 32 * kEpiStride * 4;    // int [2][BN] (FINALIZE token table, double-buffered)
+  static constexpr int tok_w = tok_t + 2 * BN * 4;           // float [2][BN]
+  static constexpr int bars = tok_w + 2 * BN * 4;            // uint64 [3*kStages + 2*kAccBufs + 1]
   static constexpr int misc = bars + (3 * kStages + 2 * kAccBufs + 1) * 8;  // tmem base, abort flag
   static constexpr int last = misc + 16;                     // int [kProducers][kStages]
   static constexpr int sched = last + kProducers * kStages * 4;  // int [3][kMaxExperts+1]
@@ -505,13 +505,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float alpha = x_scale * __ldg(p.w_scale + d.e);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAccCols;
+      int* tok_tab = s_tok_t + (acc_i & 1) * BN;
+      float* w_tab = s_tok_w + (acc_i & 1) * BN;
       if (p.epilogue == MOE_EPI_FINALIZE) {
+        // Token table of this unit: routed row et -> destination row (token, or
+        // expanded item when gathering) and router weight x alpha.  Double-buffered:
+        // the barrier below also orders the reads of the other buffer two units
+        // back before this write.
         if (et < d.rows) {
           const int ex = __ldg(p.perm_to_expanded + d.m_off + et);
           const bool in_range = ex >= 0 && ex < p.T * p.k;
           if (!in_range) record_error(p.err, MOE_ERR_INVALID_ARG, 6);
-          s_tok_t[et] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
-          s_tok_w[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
+          tok_tab[et] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
+          w_tab[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
         }
         epi_bar();
       }
@@ -529,28 +535,47 @@ __global__ void __launch_bounds__(kThreads, 1)
               out[static_cast<int64_t>(d.x_row + j0 + jj) * N + col] =
                   float_to_bf16_bits(alpha * __uint_as_float(r[jj]));
         } else if (p.epilogue == MOE_EPI_FINALIZE) {
-          // Transpose the chunk through shared memory so each thread owns 4
-          // consecutive output columns of one routed row: one 16-byte vector
-          // atomic (or store) per 4 outputs, a warp covering 512 contiguous bytes.
+          // 4x4 transposes inside each lane quad (two shuffle rounds) give lane
+          // 4g+i the four consecutive output columns 32q+4g .. +3 of routed rows
+          // i, i+4, ..., i+28 of the chunk: one 16-byte vector atomic (or store)
+          // per 4 outputs, a warp covering four 128-byte runs per instruction,
+          // with no shared-memory round trip or barrier.
+          const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) s_epi[jj * kEpiStride + m] = __uint_as_float(r[jj]);
-          epi_bar();
-          float* acc = static_cast<float*>(p.out);
-          const int64_t col0 = static_cast<int64_t>(d.mt) * kBM + 4 * lane;
-#pragma unroll 2
-          for (int jj = (et >> 5); jj < jn; jj += 4) {
-            const int tok = s_tok_t[j0 + jj];
-            if (tok < 0) continue;
-            const float w = s_tok_w[j0 + jj];
-            const float4 a = *reinterpret_cast<const float4*>(s_epi + jj * kEpiStride + 4 * lane);
-            const float4 v = make_float4(w * a.x, w * a.y, w * a.z, w * a.w);
-            float4* dst = reinterpret_cast<float4*>(acc + static_cast<int64_t>(tok) * N + col0);
-            if (p.fin_gather)
-              *dst = v;
-            else
-              atomicAdd(dst, v);
+          for (int sb = 0; sb < 8; ++sb) {
+            float a0 = __uint_as_float(r[4 * sb]), a1 = __uint_as_float(r[4 * sb + 1]);
+            float a2 = __uint_as_float(r[4 * sb + 2]), a3 = __uint_as_float(r[4 * sb + 3]);
+            // rows {0,1} x cols {2,3} <-> rows {2,3} x cols {0,1}
+            float t0 = __shfl_xor_sync(0xffffffffu, b1 ? a0 : a2, 2);
+            float t1 = __shfl_xor_sync(0xffffffffu, b1 ? a1 : a3, 2);
+            if (b1) { a0 = t0; a1 = t1; } else { a2 = t0; a3 = t1; }
+            // then within each 2x2 block
+            t0 = __shfl_xor_sync(0xffffffffu, b0 ? a0 : a1, 1);
+            t1 = __shfl_xor_sync(0xffffffffu, b0 ? a2 : a3, 1);
+            if (b0) { a0 = t0; a2 = t1; } else { a1 = t0; a3 = t1; }
+            r[4 * sb] = __float_as_uint(a0);
+            r[4 * sb + 1] = __float_as_uint(a1);
+            r[4 * sb + 2] = __float_as_uint(a2);
+            r[4 * sb + 3] = __float_as_uint(a3);
           }
-          epi_bar();
+          float* acc = static_cast<float*>(p.out) + static_cast<int64_t>(d.mt) * kBM + 32 * q + 4 * (lane >> 2);
+#pragma unroll
+          for (int sb = 0; sb < 8; ++sb) {
+            const int jj = 4 * sb + (lane & 3);
+            if (jj < jn) {
+              const int tok = tok_tab[j0 + jj];
+              if (tok >= 0) {
+                const float w = w_tab[j0 + jj];
+                const float4 v = make_float4(w * __uint_as_float(r[4 * sb]), w * __uint_as_float(r[4 * sb + 1]),
+                                             w * __uint_as_float(r[4 * sb + 2]), w * __uint_as_float(r[4 * sb + 3]));
+                float4* dst = reinterpret_cast<float4*>(acc + static_cast<int64_t>(tok) * N);
+                if (p.fin_gather)
+                  *dst = v;
+                else
+                  atomicAdd(dst, v);
+              }
+            }
+          }
         } else {
           // gate_up tile: rows 0-63 are gate rows, rows 64-127 the matching up rows.
           // Stage the chunk (128 tile rows x 32 routed rows) in shared memory, then
@@ -591,7 +616,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           epi_bar();
         }
       }
-      if (p.epilogue == MOE_EPI_FINALIZE) epi_bar();  // the token table is rewritten by the next unit
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);
     }
