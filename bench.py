@@ -42,7 +42,7 @@ METRIC = "MoE-layer tokens/s and grouped-GEMM TFLOPS & HBM GB/s vs roofline, 1 G
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tokens", type=int, default=T_DEF)
@@ -52,9 +52,10 @@ def parse():
     ap.add_argument("--intermediate", type=int, default=I_DEF)
     ap.add_argument("--zipf", type=float, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="layer", choices=["layer", "gemm"],
+    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "dense"],
                     help="layer: the full MoE layer (default); gemm: one grouped GEMM, 256 experts x 32 rows, "
-                         "K=6144, N=2048, NONE epilogue")
+                         "K=6144, N=2048, NONE epilogue; dense: one dense NVFP4 GEMM M=N=K=--dense-size")
+    ap.add_argument("--dense-size", type=int, default=16384)
     ap.add_argument("--profile-steps", action="store_true",
                     help="no JSON; only the steps run between cudaProfilerStart/Stop (for ncu)")
     return ap.parse_args()
@@ -100,28 +101,44 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
-        self.lines = []
+        self.lines = []          # (host time, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a moment to start: wait (bounded) for its first sample
+            deadline = time.time() + 5.0
+            while not self.lines and time.time() < deadline and self.proc.poll() is None:
+                time.sleep(0.005)
         except Exception:
             self.proc = None
         return self
 
+    def start(self):
+        """Marks the start of the timed region (host clock)."""
+        self.t0 = time.time()
+
+    def stop(self):
+        """Marks the end of the timed region (after the closing synchronize)."""
+        self.t1 = time.time()
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc is not None:
+            # one more sample interval so a sample lands after the region ends
+            time.sleep(2 * self.interval_ms / 1e3)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -131,7 +148,16 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        window = "timed region"
+        chosen = self.lines
+        if self.t0 is not None and self.t1 is not None:
+            # a line is printed when its sample is taken: keep those inside the timed region
+            chosen = [(t, ln) for t, ln in self.lines if self.t0 <= t <= self.t1]
+            if not chosen:
+                after = [(t, ln) for t, ln in self.lines if t > self.t1]
+                chosen = after[:1]
+                window = "first sample after the timed region (region shorter than the sampling interval)"
+        for _, ln in chosen:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -146,7 +172,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": window}
 
 
 # ------------------------------------------------------------------ setup
@@ -198,8 +224,11 @@ def algorithmic_bytes(expert_counts, T, E, k, H, I):
 
 # ------------------------------------------------------------------ CPU oracle sample
 
-def oracle_sample(x, logits, T, E, k, H, I, n_tokens, h_scale, dev):
-    """Time the CPU oracle on the first n_tokens tokens of the batch (weights of their experts only)."""
+def oracle_sample(x, logits, T, E, k, H, I, n_tokens, h_scale, dev, cache=None):
+    """Time the CPU oracle on the first n_tokens tokens of the batch (weights of their experts only).
+
+    `cache` (a dict) keeps the oracle's quantised expert weights between calls: preparing them is model
+    setup, untimed either way."""
     import oracle
     from nvfp4_moe_grouped_gb300 import inputs
 
@@ -207,8 +236,12 @@ def oracle_sample(x, logits, T, E, k, H, I, n_tokens, h_scale, dev):
     ls = logits[:n_tokens].numpy()
     ids, _ = oracle.route(ls, k)
     experts = sorted(set(ids.reshape(-1).tolist()))
-    wq13, wq2 = {}, {}
+    if cache is None:
+        cache = {}
+    wq13, wq2 = cache.setdefault("w13", {}), cache.setdefault("w2", {})
     for e in experts:   # untimed: model preparation (the FP32 weights are redrawn with the same seeds)
+        if e in wq13:
+            continue
         w13 = inputs.expert_weight(e, 2 * I, H, inputs.gate_up_seed_base(), device=dev).cpu().numpy()
         w2 = inputs.expert_weight(e, H, I, inputs.down_seed_base(E), device=dev).cpu().numpy()
         wq13[e] = oracle.quantize_dynamic(w13)
@@ -256,11 +289,12 @@ def run_reference(args, rank, world):
     logits = inputs.router_logits(T, E, zipf_s=args.zipf)
     n_tok = 1
     h_scale = 0.01
+    cache = {}
     for _ in range(args.warmup):
-        oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev)
+        oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev, cache)
     times = []
     for _ in range(args.steps):
-        dt, _ = oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev)
+        dt, _ = oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev, cache)
         times.append(dt)
     tot = sum(times)
     value = n_tok * args.steps / tot
@@ -415,6 +449,7 @@ def run_ours(args, rank, world, local_rank):
     flush = weight_bytes < (256 << 20)
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        clk.start()
         if flush:
             # the weights would stay in L2 between steps: write a 256 MB buffer before every step and
             # time each step on its own
@@ -427,6 +462,7 @@ def run_ours(args, rank, world, local_rank):
                 graph.launch()
                 b_.record(stream)
             torch.cuda.synchronize()
+            clk.stop()
             ms = sum(a_.elapsed_time(b_) for a_, b_ in ev)
         else:
             g0.record(stream)
@@ -434,6 +470,7 @@ def run_ours(args, rank, world, local_rank):
                 graph.launch()
             g1.record(stream)
             torch.cuda.synchronize()
+            clk.stop()
             ms = g0.elapsed_time(g1)
     if world > 1:
         torch.distributed.barrier()
@@ -586,11 +623,13 @@ def run_gemm(args, rank, world, local_rank):
         return
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
+        clk.start()
         a.record(stream)
         for _ in range(args.steps):
             step()
         b.record(stream)
         torch.cuda.synchronize()
+        clk.stop()
     ms = a.elapsed_time(b) / args.steps
     w_bytes = E * N * (K // 2 + K // 16)
     alg = w_bytes + R * (K // 2 + K // 16) + R * N * 2
@@ -612,6 +651,73 @@ def run_gemm(args, rank, world, local_rank):
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 
+def run_dense(args, rank, world, local_rank):
+    """One dense NVFP4 GEMM, M = N = K = --dense-size (a 'very large matrices' measurement), BF16 out,
+    against this GPU's measured dense FP4 MMA rate."""
+    import nvfp4_moe_grouped_gb300 as moe
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    M = N = K = args.dense_size
+    alloc = (M + 127) // 128 * 128
+    x = inputs.activations(M, K, seed=0, device=dev)
+    codes, sf, s = moe.nvfp4_quantize(x, None, sf_layout=moe.SF_TILED, dst_rows_alloc=alloc)
+    del x
+    wf = inputs.expert_weights(1, N, K, 900, device=dev)
+    pw = moe.prepare_expert_weights(wf, gate_up=False)
+    del wf
+    torch.cuda.empty_cache()
+    out = torch.zeros(alloc, N, dtype=torch.bfloat16, device=dev)
+    in_bytes = alloc * (K // 2 + K // 16) + N * (K // 2 + K // 16)
+    l2_flush = in_bytes < (256 << 20)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if l2_flush else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.dense_gemm_nvfp4(codes, sf, s, pw, M, out=out)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if args.profile_steps:
+        torch.cuda.cudart().cudaProfilerStart()
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        return
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        clk.start()
+        for a, b in evs:
+            if flush is not None:
+                flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        clk.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    flops = 2.0 * M * N * K
+    tf = flops / (ms / 1e3) / 1e12
+    peak_fp4 = moe.fp4_mma_peak_tflops()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "dense NVFP4 GEMM TFLOPS vs dense FP4 peak", "value": tf, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e2m1xe2m1->f32",
+            "data": "synthetic",
+            "config": {"workload": f"dense_gemm_M{M}_N{N}_K{K}_bf16out",
+                       "l2": ("256 MB written between timed launches (inputs fit in L2)" if l2_flush
+                              else f"inputs ({in_bytes / 2**20:.0f} MB) exceed L2; no flush")},
+            "roofline": {"bound": "tensor", "kernel": "grouped_gemm NONE (one group)", "achieved": tf,
+                         "peak": peak_fp4, "unit": "TFLOP/s", "frac": tf / peak_fp4,
+                         "peak_kind": "measured (this GPU's dense NVFP4 MMA rate, moe_fp4_mma_probe)",
+                         "traffic": None, "algorithmic_flops_per_launch": flops, "launch_ms": ms},
+            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -625,6 +731,8 @@ def main():
     try:
         if args.workload == "gemm":
             run_gemm(args, rank, world, local_rank)
+        elif args.workload == "dense":
+            run_dense(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

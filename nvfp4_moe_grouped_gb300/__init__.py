@@ -240,6 +240,17 @@ def moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, w: PreparedWeights, expert_of
     return out
 
 
+def dense_gemm_nvfp4(a_codes, a_sf, a_scale, w: PreparedWeights, M: int, out=None, stream=None):
+    """Dense NVFP4 GEMM C[M][N] = A[M][K] . B[N][K]^T (BF16 out): the grouped GEMM with one group.
+
+    A is in the padded-row layout with tiled scales (rows_alloc = a_codes.shape[0] >= M, a multiple
+    of 128), `w` one prepared matrix (E = 1).  Returns C over rows_alloc rows (rows >= M untouched)."""
+    if w.E != 1:
+        raise ValueError("dense_gemm_nvfp4 takes one prepared matrix (E = 1)")
+    offs = torch.tensor([0, M], dtype=torch.int32, device=a_codes.device)
+    return moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, w, offs, EPI_NONE, out=out, stream=stream)
+
+
 def moe_finalize(y: torch.Tensor, topk_w: torch.Tensor, row_of_item: torch.Tensor, out=None, stream=None):
     T, k = topk_w.shape
     N = y.shape[1]

@@ -61,6 +61,41 @@ def test_c2_grouped_gemm_none_full_size_sampled():
     assert np.count_nonzero(np.abs(got[dst]).sum(1) == 0) == 0
 
 
+# ------------------------------------------------------------------ dense NVFP4 GEMM (the bench's dense workload)
+
+def test_dense_gemm_full_size_sampled():
+    """M = N = K = 16384 through dense_gemm_nvfp4 (one group), as `bench.py --workload dense` times it."""
+    M = N = K = 16384
+    x = inputs.activations(M, K, seed=0, device=DEV)
+    codes, sf, s = moe.nvfp4_quantize(x, None, sf_layout=moe.SF_TILED, dst_rows_alloc=M)
+    rng = np.random.default_rng(3)
+    rs = np.sort(rng.choice(M, 8, replace=False))
+    xh = x.cpu().float().numpy()          # exact widening of the bf16 draw, on the host
+    del x
+    wf = inputs.expert_weights(1, N, K, 900, device=DEV)
+    pw = moe.prepare_expert_weights(wf, gate_up=False)
+    wh = wf[0].cpu().numpy()
+    del wf
+    torch.cuda.empty_cache()
+    out = moe.dense_gemm_nvfp4(codes, sf, s, pw, M)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    # oracle: per-tensor multipliers from the host copies, then the sampled rows quantised with them
+    ns = np.sort(rng.choice(N, 48, replace=False))
+    xsc = oracle.tensor_scale_from_amax(oracle.amax(xh))
+    wsc = oracle.tensor_scale_from_amax(oracle.amax(wh))
+    assert np.float32(xsc) == s.item() and np.float32(wsc) == pw.scale[0].item()
+    xc, xsf = oracle.quantize(xh[rs], xsc)
+    wc, wsf = oracle.quantize(wh[ns], wsc)
+    del xh, wh
+    assert np.array_equal(codes[torch.from_numpy(rs).to(DEV)].cpu().numpy(), xc)
+    ref = np.array([[oracle.gemm_element(xc[i], xsf[i], xsc, wc[j], wsf[j], wsc) for j in range(len(ns))]
+                    for i in range(len(rs))])
+    got = bf16_to_np(out[torch.from_numpy(rs).to(DEV)])[:, ns]
+    tol_check(got, ref, "dense GEMM 16384^3")
+    assert np.count_nonzero(np.abs(bf16_to_np(out[:M:1024])).sum(1) == 0) == 0
+
+
 # ------------------------------------------------------------------ C3/C4/C5: the layer
 
 @pytest.fixture(scope="module")
