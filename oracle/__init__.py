@@ -70,6 +70,9 @@ def lib():
                                      ctypes.c_void_p]
         L.orc_exp.restype = ctypes.c_float
         L.orc_exp.argtypes = [ctypes.c_float]
+        L.orc_router_logits.restype = None
+        L.orc_router_logits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p]
         L.orc_route.restype = ctypes.c_int
         L.orc_route.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_void_p, ctypes.c_void_p]
@@ -189,6 +192,20 @@ def dequantize(codes: np.ndarray, sf: np.ndarray) -> np.ndarray:
     K = codes.shape[1] * 2
     out = np.empty((rows, K), np.float64)
     lib().orc_dequantize(_p(codes), _p(sf), rows, K, _p(out))
+    return out
+
+
+def router_logits(x: np.ndarray, w_gate: np.ndarray) -> np.ndarray:
+    """logits[t][e] = sum_h x[t][h] * w_gate[e][h] in FP64, rounded once to FP32 (reading R8).
+
+    x [T][H] and w_gate [E][H] hold bf16 values (any float dtype that represents them exactly)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    w = np.ascontiguousarray(w_gate, dtype=np.float32)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H
+    out = np.zeros((T, E), np.float32)
+    lib().orc_router_logits(_p(x), _p(w), T, E, H, _p(out))
     return out
 
 

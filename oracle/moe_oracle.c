@@ -46,6 +46,8 @@
  *  R6 SiLU-mul: h = g / (1 + e^-g) * u with gate rows [0, I) and up rows
  *     [I, 2I) of the gate_up output; requantised with a given static scale.
  *  R7 FINALIZE: out[t] = sum_j w[t,j] * Y[row(t,j)], rounded once to bf16.
+ *  R8 router logits: a bias-free linear gate, logits[t][e] = sum_h x[t][h] *
+ *     w_gate[e][h] over bf16 inputs, summed in FP64 and rounded once to FP32.
  *
  * Parity status: every exported function is pinned by tests/test_oracle_*.py
  * against closed forms, library routines or brute force.
@@ -199,6 +201,23 @@ EXPORT float orc_exp(float x) {
   two_n.u = (uint32_t)((int)n + 127) << 23;
   volatile float res = p * two_n.f;
   return res;
+}
+
+/* ------------------------------------------------------------------ */
+/* Router logits (R8).  "Tracing the Failure: Debugging CUTLASS FP4     */
+/* Tile Configurations on Blackwell SM120", "The Broader Context":      */
+/* each token is scored against every expert before the top-k.          */
+/* ------------------------------------------------------------------ */
+
+/* x: [T][H], w: [E][H] (the bf16 values, widened to float); out: [T][E]. */
+EXPORT void orc_router_logits(const float* x, const float* w, int T, int E, int H, float* out) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h) acc += (double)x[(int64_t)t * H + h] * (double)w[(int64_t)e * H + h];
+      out[(int64_t)t * E + e] = (float)acc;
+    }
 }
 
 /* ------------------------------------------------------------------ */

@@ -222,3 +222,49 @@ def test_full_layer_c1_against_fp64_restatement():
     # FP32 h decides the same codes), so agreement is to FP64 rounding.
     assert np.allclose(res.out, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
     assert np.abs(ref).max() > 0
+
+
+# ------------------------------------------------------------------ router logits (reading R8)
+
+def _bf16_round(a):
+    """Round float32 values to bf16 (nearest even) and back, so they are exact bf16 values."""
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16 << 16
+    return u.astype(np.uint32).view(np.float32)
+
+
+def test_router_logits_one_hot_gate_selects_columns():
+    """Expert e's gate row is the unit vector of hidden index j(e): logits are the selected x columns, exactly."""
+    rng = np.random.default_rng(5)
+    T, H, E = 7, 96, 12
+    x = _bf16_round(rng.standard_normal((T, H)).astype(np.float32))
+    cols = rng.choice(H, E, replace=False)
+    w = np.zeros((E, H), np.float32)
+    w[np.arange(E), cols] = 1.0
+    assert np.array_equal(oracle.router_logits(x, w), x[:, cols])
+
+
+def test_router_logits_constant_inputs_closed_form():
+    """x = 1 everywhere, gate row e constant c_e: logit = H * c_e (exact in FP32 for these c_e)."""
+    T, H, E = 3, 640, 5
+    c = np.array([0.5, -0.25, 1.5, 0.0, -3.0], np.float32)
+    x = np.ones((T, H), np.float32)
+    w = np.repeat(c[:, None], H, axis=1)
+    assert np.array_equal(oracle.router_logits(x, w), np.tile(H * c, (T, 1)).astype(np.float32))
+
+
+def test_router_logits_brute_force_small_integers():
+    """Small integer inputs: every product and sum is exact, checked against plain Python loops."""
+    rng = np.random.default_rng(9)
+    T, H, E = 4, 9, 6
+    x = rng.integers(-8, 9, (T, H)).astype(np.float32)
+    w = rng.integers(-8, 9, (E, H)).astype(np.float32)
+    ref = [[sum(int(x[t, h]) * int(w[e, h]) for h in range(H)) for e in range(E)] for t in range(T)]
+    assert np.array_equal(oracle.router_logits(x, w), np.array(ref, np.float32))
+
+
+def test_router_logits_single_rounding_to_fp32():
+    """The sum is formed in FP64 and rounded once: 1 + 2^-30 - 1 keeps the 2^-30 an FP32 running sum would lose."""
+    x = np.array([[1.0, 2.0 ** -15, -1.0]], np.float32)
+    w = np.array([[1.0, 2.0 ** -15, 1.0]], np.float32)
+    assert oracle.router_logits(x, w)[0, 0] == np.float32(2.0 ** -30)
