@@ -52,9 +52,10 @@ def parse():
     ap.add_argument("--intermediate", type=int, default=I_DEF)
     ap.add_argument("--zipf", type=float, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "dense"],
+    ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "dense", "router"],
                     help="layer: the full MoE layer (default); gemm: one grouped GEMM, 256 experts x 32 rows, "
-                         "K=6144, N=2048, NONE epilogue; dense: one dense NVFP4 GEMM M=N=K=--dense-size")
+                         "K=6144, N=2048, NONE epilogue; dense: one dense NVFP4 GEMM M=N=K=--dense-size; "
+                         "router: the router logits GEMM + routing for --tokens tokens")
     ap.add_argument("--dense-size", type=int, default=16384)
     ap.add_argument("--profile-steps", action="store_true",
                     help="no JSON; only the steps run between cudaProfilerStart/Stop (for ncu)")
@@ -718,6 +719,70 @@ def run_dense(args, rank, world, local_rank):
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 
+def run_router(args, rank, world, local_rank):
+    """The router: logits GEMM x . w_gate^T (bf16, tcgen05) + top-k routing and permutation."""
+    import nvfp4_moe_grouped_gb300 as moe
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T, E, k, H = args.tokens, args.experts, args.top_k, args.hidden
+    x = inputs.activations(T, H, seed=0, device=dev)
+    wg = inputs.router_gate(E, H, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # inputs fit in L2
+    r, _ = moe.moe_router(x, wg, k, want_logits=False)
+    ws = torch.empty(moe._lib.load().moe_router_workspace_size(T, E, H, k), dtype=torch.uint8, device=dev)
+    for _ in range(max(1, args.warmup)):
+        moe.moe_router(x, wg, k, want_logits=False, out=r, ws=ws)
+    torch.cuda.synchronize()
+    if args.profile_steps:
+        torch.cuda.cudart().cudaProfilerStart()
+        for _ in range(args.steps):
+            moe.moe_router(x, wg, k, want_logits=False, out=r, ws=ws)
+        torch.cuda.synchronize()
+        torch.cuda.cudart().cudaProfilerStop()
+        return
+    # the call as one CUDA graph, so host-side marshalling between launches is not timed
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        moe.moe_router(x, wg, k, want_logits=False, out=r, ws=ws, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        graph.replay()
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        clk.start()
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        clk.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    alg = T * H * 2 + E * H * 2 + 2 * T * E * 4 + T * k * (4 + 4 + 4 * 3) + (E + 1) * 4
+    gbs = alg / (ms / 1e3) / 1e9
+    hbm_peak, _, peak_kind = peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "router (logits GEMM + top-k + permutation) tokens/s", "value": T / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16xbf16->f32",
+            "data": "synthetic",
+            "config": {"workload": f"router_T{T}_E{E}_k{k}_H{H}",
+                       "l2": "256 MB written between timed calls (inputs fit in L2)"},
+            "roofline": {"bound": "hbm", "kernel": "router (5 launches)", "achieved": gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg, "launch_ms": ms},
+            "gpu_launches": 5 * args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -733,6 +798,8 @@ def main():
             run_gemm(args, rank, world, local_rank)
         elif args.workload == "dense":
             run_dense(args, rank, world, local_rank)
+        elif args.workload == "router":
+            run_router(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -174,6 +174,35 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
                                     int32_t* expanded_to_row, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_router -- the router in front of moe_route_permute: the logits GEMM
+ *   logits[t][e] = sum_h x[t][h] * w_gate[e][h]
+ * on the tensor cores (bf16 inputs, FP32 sums), then moe_route_permute on
+ * those logits.
+ *   "Tracing the Failure: Debugging CUTLASS FP4 Tile Configurations on
+ *   Blackwell SM120", "The Broader Context" (each token scored against 256
+ *   experts, 8 kept).  The pages give no gate formula: this is a bias-free
+ *   linear gate.
+ * The K = H sum is split into contiguous ranges whose FP32 partial sums are
+ * added in range order, so the logits (and everything routed from them) are
+ * the same on every call with the same inputs; they differ from a sequential
+ * sum only by FP32 rounding order.
+ * Arguments (device pointers unless noted):
+ *   x        bf16 [T][H] (raw bits), 16-byte aligned
+ *   w_gate   bf16 [E][H], 16-byte aligned
+ *   logits   f32 [T][E] out, or NULL (not written: the routing kernel adds
+ *            the partial sums as it reads them)
+ *   topk_id ... expanded_to_row   as moe_route_permute
+ *   ws / ws_bytes  workspace of moe_router_workspace_size(T, E, H, k) bytes,
+ *                  queried with the device that will run the call current
+ * Requires 1 <= k <= min(E, 32), E <= 256, H a multiple of 64, T >= 1.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_router_workspace_size(int T, int E, int H, int k);
+MOE_API moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int T, int E, int H, int k, float* logits,
+                              int32_t* topk_id, float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
+                              int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* ---------------------------------------------------------------------------
  * nvfp4_quantize -- NVFP4 quantisation of rows of a bf16 or f32 matrix.
  *   "Cracking the SM120 Shared Memory Ceiling ...", "The Shared Memory
  *   Calculation" (4-bit values, one FP8 scale per 16 elements along K).

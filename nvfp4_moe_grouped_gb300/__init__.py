@@ -119,6 +119,38 @@ def moe_route_permute(logits: torch.Tensor, k: int, stream=None) -> Routing:
     return r
 
 
+def moe_router(x: torch.Tensor, w_gate: torch.Tensor, k: int, want_logits: bool = True, stream=None,
+               out: Routing | None = None, logits: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+    """Router logits x . w_gate^T on the tensor cores (bf16 in, FP32 sums), then moe_route_permute.
+
+    `out`, `logits` and `ws` may be given preallocated (e.g. for graph capture).
+    Returns (Routing, logits f32 [T][E] or None)."""
+    if x.dtype != torch.bfloat16 or w_gate.dtype != torch.bfloat16:
+        raise TypeError("x and w_gate must be bf16")
+    x = x.contiguous()
+    w_gate = w_gate.contiguous()
+    T, H = x.shape
+    E = w_gate.shape[0]
+    dev = x.device
+    R = T * k
+    r = out if out is not None else Routing(
+        _empty((T, k), torch.int32, dev), _empty((T, k), torch.float32, dev), _empty(E + 1, torch.int32, dev),
+        _empty(R, torch.int32, dev), _empty(R, torch.int32, dev), _empty(R, torch.int32, dev))
+    if logits is None and want_logits:
+        logits = _empty((T, E), torch.float32, dev)
+    L = _L()
+    wsb = L.moe_router_workspace_size(T, E, H, k)
+    if ws is None:
+        ws = _empty(max(wsb, 256), torch.uint8, dev)
+    elif ws.numel() < wsb:
+        raise ValueError("router workspace too small")
+    _check("moe_router", L.moe_router(
+        _ptr(x), _ptr(w_gate), T, E, H, k, _ptr(logits), _ptr(r.topk_id), _ptr(r.topk_w), _ptr(r.expert_offsets),
+        _ptr(r.perm_to_expanded), _ptr(r.expanded_to_perm), _ptr(r.expanded_to_row), _ptr(ws), wsb,
+        _stream(stream)))
+    return r, logits
+
+
 # ---------------------------------------------------------------- quantisation
 
 def nvfp4_quantize(x: torch.Tensor, tensor_scale: torch.Tensor | None = None, groups: int = 1,

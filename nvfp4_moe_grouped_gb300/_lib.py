@@ -58,6 +58,8 @@ SIGNATURES = {
     "moe_blocked_weight_bytes": (c_size_t, [c_int64, c_int]),
     "moe_route_permute_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_route_permute": (c_int, [c_void_p, c_int, c_int, c_int] + [c_void_p] * 7 + [c_size_t, c_void_p]),
+    "moe_router_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "moe_router": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int] + [c_void_p] * 8 + [c_size_t, c_void_p]),
     "moe_route_permute_static_scratch_bytes": (c_size_t, []),
     "moe_route_permute_static": (c_int, [c_void_p, c_int, c_int, c_int] + [c_void_p] * 7),
     "nvfp4_quantize_workspace_size": (c_size_t, [c_int]),

@@ -24,6 +24,11 @@ int32_t* device_error_word();          // device address of {code, where}
 uint64_t wait_timeout_ns();            // bound of every device-side wait
 int num_sms();                          // SM count of the current device
 moe_status check_launch();              // maps cudaGetLastError to a status
+// cuTensorMapEncodeTiled from the driver, or nullptr when the driver lacks it.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -228,6 +233,17 @@ MOE_DEVINL void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, 
       : "memory");
 }
 
+// D (TMEM, FP32) (+)= A (smem, bf16, K-major) x B (smem, bf16, K-major)^T: one
+// tcgen05.mma of kind::f16 (M = 128, K = 16); A and B are both bf16.
+MOE_DEVINL void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 MOE_DEVINL void mma_commit(uint64_t* bar) {
@@ -284,6 +300,13 @@ MOE_DEVINL uint64_t smem_desc(uint32_t start, uint32_t lbo, uint32_t sbo, uint32
 // K-major, ue4m3 scales (bit 23 = 0), dense, M = 128.
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int n) {
   return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B (format 1), FP32 D
+// (bits 4-5 = 1), both K-major, dense, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
 }  // namespace moe

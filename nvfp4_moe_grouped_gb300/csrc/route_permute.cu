@@ -39,11 +39,20 @@ inline RouteDims route_dims(int T, int E, int k) {
 // Larger of two (value, index) candidates: higher value, then lower index.
 MOE_DEVINL bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-template <int NV>  // logits per lane: NV * 32 >= E
+// Logits given as FP32 partial sums over K ranges (the router's split GEMM):
+// logit[t][e] = sum over s, in order, of part[t / 128][s][t % 128][e].
+struct PartialLogits {
+  const float* part;  // [tiles][splits][128][NE]
+  int splits, NE;
+  float* logits_out;  // optional copy of the summed logits, [T][E]
+};
+
+template <int NV, bool PARTS>  // NV: logits per lane, NV * 32 >= E; PARTS: read partial sums
 __global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __restrict__ logits, RouteDims d,
                                                               int32_t* __restrict__ topk_id,
                                                               float* __restrict__ topk_w,
-                                                              int32_t* __restrict__ chunk_counts) {
+                                                              int32_t* __restrict__ chunk_counts,
+                                                              PartialLogits pl) {
   extern __shared__ int hist[];  // [E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * d.chunk_tokens;
@@ -58,8 +67,25 @@ __global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __rest
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       int e = lane + 32 * i;
-      if (e < d.E) v[i] = __ldg(row + e);
-      else { v[i] = 0.0f; taken |= 1u << i; }
+      v[i] = 0.0f;
+      if (e >= d.E) taken |= 1u << i;
+      else if (!PARTS) v[i] = __ldg(row + e);
+    }
+    if (PARTS) {
+      // splits outermost, so each step issues the NV independent loads of all the lane's experts
+      const float* src = pl.part + (static_cast<int64_t>(t >> 7) * pl.splits * 128 + (t & 127)) * pl.NE + lane;
+#pragma unroll 8
+      for (int sp = 0; sp < pl.splits; ++sp) {
+        const float* s_row = src + static_cast<int64_t>(sp) * 128 * pl.NE;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (lane + 32 * i < d.E) v[i] = __fadd_rn(v[i], __ldg(s_row + 32 * i));
+      }
+      if (pl.logits_out) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (lane + 32 * i < d.E) pl.logits_out[static_cast<int64_t>(t) * d.E + lane + 32 * i] = v[i];
+      }
     }
     float my_v = 0.0f;
     int my_i = 0;
@@ -206,24 +232,22 @@ int32_t* route_pad_offsets(void* ws, int T, int E, int k) {
 }
 }  // namespace moe
 
-extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* topk_id, float* topk_w,
-                                        int32_t* expert_offsets, int32_t* perm_to_expanded,
-                                        int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws,
-                                        size_t ws_bytes, void* stream) {
-  if (!logits || !topk_id || !topk_w || !expert_offsets || !perm_to_expanded || !expanded_to_perm ||
-      !expanded_to_row)
-    return MOE_ERR_INVALID_ARG;
-  if (T < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
-  if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < moe_route_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace moe {
+// Routing and permutation from full logits, or (part != nullptr) from the
+// router GEMM's partial sums.  Arguments are validated by the callers.
+moe_status route_permute_enqueue(const float* logits, const float* part, int splits, int NE, float* logits_out,
+                                 int T, int E, int k, int32_t* topk_id, float* topk_w, int32_t* expert_offsets,
+                                 int32_t* perm_to_expanded, int32_t* expanded_to_perm, int32_t* expanded_to_row,
+                                 void* ws, cudaStream_t st) {
   RouteDims d = route_dims(T, E, k);
   int32_t* counts = static_cast<int32_t*>(ws);
   int32_t* pads = route_pad_offsets(ws, T, E, k);
   const size_t hist_bytes = sizeof(int) * E;
   const int nv = (E + 31) / 32;
-#define MOE_ROUTE(NV) route_kernel<NV><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts)
+  const PartialLogits pl{part, splits, NE, logits_out};
+#define MOE_ROUTE(NV)                                                                                         \
+  (part ? route_kernel<NV, true><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl) \
+        : route_kernel<NV, false><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl))
   if (nv <= 1) MOE_ROUTE(1);
   else if (nv <= 2) MOE_ROUTE(2);
   else if (nv <= 4) MOE_ROUTE(4);
@@ -235,4 +259,21 @@ extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k
   scatter_kernel<<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(d, topk_id, counts, expert_offsets, pads,
                                                                 perm_to_expanded, expanded_to_perm, expanded_to_row);
   return check_launch();
+}
+}  // namespace moe
+
+extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k, int32_t* topk_id, float* topk_w,
+                                        int32_t* expert_offsets, int32_t* perm_to_expanded,
+                                        int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (!logits || !topk_id || !topk_w || !expert_offsets || !perm_to_expanded || !expanded_to_perm ||
+      !expanded_to_row)
+    return MOE_ERR_INVALID_ARG;
+  if (T < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < moe_route_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
+  return route_permute_enqueue(logits, nullptr, 0, 0, nullptr, T, E, k, topk_id, topk_w, expert_offsets,
+                               perm_to_expanded, expanded_to_perm, expanded_to_row, ws,
+                               static_cast<cudaStream_t>(stream));
 }

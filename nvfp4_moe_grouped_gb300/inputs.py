@@ -46,6 +46,12 @@ def router_logits(T: int, E: int, seed: int = 1, zipf_s: float | None = None, de
     return (logp[None, :] + gumbel).to(torch.float32).to(device)
 
 
+def router_gate(E: int, H: int, seed: int = 100000, device="cpu", std: float = 0.02) -> torch.Tensor:
+    """Gate matrix w_gate [E][H] in bf16, ~N(0, std)."""
+    return (torch.randn((E, H), generator=_gen(seed, device), device=device, dtype=torch.float32) * std).to(
+        torch.bfloat16)
+
+
 def expert_weight(e: int, N: int, K: int, seed_base: int, device="cpu", std: float = 0.02) -> torch.Tensor:
     return torch.randn((N, K), generator=_gen(seed_base + e, device), device=device, dtype=torch.float32) * std
 

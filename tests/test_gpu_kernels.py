@@ -130,6 +130,37 @@ def test_finalize_matches_oracle(T, k, N):
     tol_check(bf16_to_np(out), ref, "finalize")
 
 
+# ------------------------------------------------------------------ router (logits GEMM + routing)
+
+@pytest.mark.parametrize("T,E,k,H", [(16, 8, 2, 256), (129, 40, 4, 512), (300, 256, 8, 1024), (1024, 256, 8, 6144)])
+def test_router_matches_oracle(T, E, k, H):
+    """Logits within the FP32 summation-order bound of the oracle's FP64 sums; the routing is exactly the
+    oracle's routing of the GPU's logits, and agrees with the oracle's own logits except at near-ties."""
+    x = inputs.activations(T, H, seed=T)
+    wg = inputs.router_gate(E, H)
+    r, lg = moe.moe_router(x.to(DEV), wg.to(DEV), k)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    xf, wf = x.float().numpy(), wg.float().numpy()
+    ref = oracle.router_logits(xf, wf)
+    got = lg.cpu().numpy()
+    bound = 4.0 * H * 2.0 ** -24 * (np.abs(xf).astype(np.float64) @ np.abs(wf).astype(np.float64).T)
+    assert np.all(np.abs(got.astype(np.float64) - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
+    ids, w = oracle.route(got, k)
+    offs, p2e, e2p = oracle.permute(ids, E)
+    assert np.array_equal(r.topk_id.cpu().numpy(), ids)
+    assert np.array_equal(r.topk_w.cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(r.expert_offsets.cpu().numpy(), offs)
+    assert np.array_equal(r.perm_to_expanded.cpu().numpy(), p2e)
+    assert np.array_equal(r.expanded_to_perm.cpu().numpy(), e2p)
+    # against the oracle's logits: a token may select differently only where its k-th and (k+1)-th
+    # oracle logits are closer than the summation bound allows to separate
+    ids_ref, _ = oracle.route(ref, k)
+    for t in np.nonzero(np.any(np.sort(ids, 1) != np.sort(ids_ref, 1), axis=1))[0]:
+        srt = np.sort(ref[t])[::-1]
+        assert srt[k - 1] - srt[k] <= 2 * bound[t].max(), t
+
+
 # ------------------------------------------------------------------ grouped GEMM
 
 def _routed_operand(x_bf16, offs):
