@@ -148,28 +148,55 @@ MOE_DEVINL int block_exclusive_scan(int v, int* warp_tot) {
   return r;
 }
 
+// One block of 1024 threads: thread (g, e) = (tid / Ep, tid % Ep), Ep = E rounded
+// up to 32, covers chunk group g of expert e (G = 1024 / Ep groups split the
+// chunks), so up to G loads per expert are in flight instead of one.
 __global__ void __launch_bounds__(1024) scan_kernel(RouteDims d, int32_t* __restrict__ chunk_counts,
                                                      int32_t* __restrict__ expert_offsets,
                                                      int32_t* __restrict__ pad_offsets) {
   __shared__ int warp_tot[32];
-  const int e = threadIdx.x;
+  __shared__ int part[1024];  // [G][Ep] per-group totals, then per-group bases
+  const int Ep = (d.E + 31) & ~31;
+  const int G = blockDim.x / Ep;
+  const int g = threadIdx.x / Ep, e = threadIdx.x - g * Ep;
+  const bool act = g < G && e < d.E;
+  const int b0 = act ? static_cast<int>(static_cast<int64_t>(g) * d.n_chunks / G) : 0;
+  const int b1 = act ? static_cast<int>(static_cast<int64_t>(g + 1) * d.n_chunks / G) : 0;
+  int sub = 0;
+#pragma unroll 8
+  for (int b = b0; b < b1; ++b) sub += chunk_counts[static_cast<int64_t>(b) * d.E + e];
+  if (g < G) part[threadIdx.x] = sub;
+  __syncthreads();
+  // group 0 holds each expert's total; thread order puts group 0 first, so the
+  // block-wide exclusive scan over (group 0 totals, zeros) gives the expert offsets
   int total = 0;
-  if (e < d.E)
-    for (int b = 0; b < d.n_chunks; ++b) total += chunk_counts[static_cast<int64_t>(b) * d.E + e];
-  int off = block_exclusive_scan(e < d.E ? total : 0, warp_tot);
-  int padded = e < d.E ? ((total + 127) / 128) * 128 : 0;
-  int poff = block_exclusive_scan(padded, warp_tot);
-  if (e < d.E) {
+  if (g == 0 && e < d.E)
+    for (int h = 0; h < G; ++h) total += part[h * Ep + e];
+  const int off = block_exclusive_scan(total, warp_tot);
+  const int padded = (g == 0 && e < d.E) ? ((total + 127) / 128) * 128 : 0;
+  const int poff = block_exclusive_scan(padded, warp_tot);
+  if (g == 0 && e < d.E) {
     expert_offsets[e] = off;
     pad_offsets[e] = poff;
     if (e == d.E - 1) {
       expert_offsets[d.E] = off + total;
       pad_offsets[d.E] = poff + padded;
     }
+    // per-group bases of this expert
     int run = off;
-    for (int b = 0; b < d.n_chunks; ++b) {
-      int64_t o = static_cast<int64_t>(b) * d.E + e;
-      int c = chunk_counts[o];
+    for (int h = 0; h < G; ++h) {
+      const int c = part[h * Ep + e];
+      part[h * Ep + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (act) {
+    int run = part[threadIdx.x];
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) {
+      const int64_t o = static_cast<int64_t>(b) * d.E + e;
+      const int c = chunk_counts[o];
       chunk_counts[o] = run;  // becomes the chunk's first position for expert e
       run += c;
     }
@@ -255,7 +282,7 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
   else if (nv <= 16) MOE_ROUTE(16);
   else MOE_ROUTE(32);
 #undef MOE_ROUTE
-  scan_kernel<<<1, ((E + 31) / 32) * 32, 0, st>>>(d, counts, expert_offsets, pads);
+  scan_kernel<<<1, 1024, 0, st>>>(d, counts, expert_offsets, pads);
   scatter_kernel<<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(d, topk_id, counts, expert_offsets, pads,
                                                                 perm_to_expanded, expanded_to_perm, expanded_to_row);
   return check_launch();

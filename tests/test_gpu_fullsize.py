@@ -200,5 +200,11 @@ def test_layer_full_size_sampled(weights, oracle_cache, T, zipf):
     _run_layer_case(weights, T, zipf, 3, oracle_cache)
 
 
+@pytest.mark.parametrize("T,zipf", [(128, 1.1), (256, None), (256, 1.1), (512, None)])
+def test_layer_c3_remaining_sizes_sampled(weights, oracle_cache, T, zipf):
+    """The rest of the decode sweep T in {128, 256, 512, 1024} x {uniform, Zipf(1.1)}."""
+    _run_layer_case(weights, T, zipf, 2, oracle_cache)
+
+
 def test_layer_prefill_full_size_sampled(weights, oracle_cache):
     _run_layer_case(weights, 16384, None, 2, oracle_cache)
