@@ -18,7 +18,7 @@
 //     weight tile is streamed from HBM once per BN routed rows and the tensor
 //     core never computes padding rows of M.
 //   * The routed-row tile BN is picked per launch from the rows-per-expert
-//     regime: BN = 64 with 7 pipeline stages for decode, BN = 128 with 5
+//     regime: BN = 64 with 7 pipeline stages for decode, BN = 128 with 4
 //     stages when experts see more rows (prefill).
 //   * Work unit = (expert, BN-row block of its routed rows, 128-row weight
 //     tile), full K.  Units are ordered expert-major so the CTAs running
@@ -31,15 +31,17 @@
 //     exact shared-memory image the MMA descriptor reads) and its four scale
 //     atoms, so each pipeline stage of weights is ONE linear bulk copy that
 //     streams a contiguous 18 KB run of HBM.
-//   * Warp roles: warps 0 and 10-12 issue the copies, each one stage fill in
-//     four (weights: bulk copy, evict-first; routed rows: 2D tensor-map loads
-//     with 128-byte swizzle and a bulk copy of their scale atoms, evict-last);
-//     one issuing thread gets its bulk copies served one after another, which
-//     caps a single producer near 5 TB/s of L2 hits per GPU.  Warps 6-9 move each
-//     stage's scale atoms from shared into tensor memory (tcgen05.st, one
-//     warp per lane quadrant), warp 1 owns tensor memory and issues only the
-//     tcgen05.mma instructions and their commits, warps 2-5 drain the
-//     accumulator (tcgen05.ld) and run the epilogue.  A tcgen05.cp of the
+//   * Warp roles: warp 0 issues the copies (weights: bulk copy, evict-first;
+//     routed rows: 2D tensor-map loads with 128-byte swizzle and a bulk copy
+//     of their scale atoms, evict-last).  In the decode tile warps 10-12 issue
+//     copies too, each one stage fill in four: one issuing thread gets its bulk
+//     copies served one after another.  Warps 6-9 move each stage's scale atoms
+//     from shared into tensor memory (tcgen05.st, one warp per lane quadrant),
+//     warp 1 owns tensor memory and issues only the tcgen05.mma instructions
+//     and their commits, warps 2-5 drain the accumulator (tcgen05.ld) and run
+//     the epilogue; in the prefill tile warps 10-13 form a second epilogue
+//     group that drains every other unit, since one group could not keep up
+//     with the FINALIZE and SiLU epilogues there.  A tcgen05.cp of the
 //     scales on the MMA thread would serialise with the MMA that reads them:
 //     at decode that halved the weight-streaming rate.  Several TMEM
 //     accumulators (four for the 64-row tile, two for the 128-row one) let the
@@ -78,17 +80,24 @@ constexpr int kBM = 128;                  // weight rows per tile (MMA M)
 constexpr int kBK = 256;                  // K elements per stage (128 bytes per row)
 constexpr int kWStageBytes = kBlockedTileBytes;  // 16 KB codes + 2 KB scale atoms
 constexpr int kSfStageBytes = 4 * 512;    // scale atoms of the routed rows (one per 64-element K step)
-constexpr int kProducers = 4;            // copy-issuing warps: 0 and 10 .. 8 + kProducers
-constexpr int kFirstExtraProducer = 10;
-constexpr int kThreads = 32 * (kFirstExtraProducer + kProducers - 1);  // 1 MMA, 2-5 epilogue, 6-9 scale staging
+constexpr int kExtraWarp = 10;           // warps 0-9: copies, MMA, epilogue 2-5, scale staging 6-9; then extras
 constexpr int kMaxExperts = 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfSlotCols = 32;      // 16 columns weight scales + 16 columns routed-row scales
-constexpr int kEpiStride = 132;           // floats per staged routed row (128 tile rows + 4: 16-byte rows, fewer bank conflicts)
+constexpr int kEpiStride = 130;           // floats per staged routed row (128 tile rows + 2: fewer bank conflicts)
 
-template <int BN>
+// EG = epilogue warp groups.  With one group, four copy-issuing warps (0,
+// 10-12) keep more bulk copies in flight.  Two groups are for a launch whose
+// epilogue is slower than its mainloop (FINALIZE at 128 routed rows: short
+// K = I units, an atomic per 4 outputs): warps 10-13 form a second group that
+// takes every other unit, so two accumulators drain at once; that launch keeps
+// one copy warp and four stages to fit the second staging buffer.
+template <int BN, int EG>
 struct Cfg {
-  static constexpr int kStages = BN == 64 ? 7 : 5;
+  static constexpr int kEpiGroups = EG;
+  static constexpr int kProducers = EG == 1 ? 4 : 1;
+  static constexpr int kThreads = 32 * (kExtraWarp + (kProducers - 1) + 4 * (kEpiGroups - 1));
+  static constexpr int kStages = BN == 64 ? 7 : (EG == 1 ? 5 : 4);
   static constexpr int kXStageBytes = BN * kBK / 2;
   static constexpr uint32_t kAccCols = BN;
   // Accumulator buffers: the epilogue of a unit may lag the mainloop by kAccBufs - 1 units
@@ -105,8 +114,8 @@ struct Cfg {
   static constexpr int w = 0;
   static constexpr int x = w + kStages * kWStageBytes;
   static constexpr int sfx = x + kStages * kXStageBytes;
-  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][kEpiStride]
-  static constexpr int tok_t = epi + 32 * kEpiStride * 4;    // int [2][BN] (FINALIZE token table, double-buffered)
+  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [kEpiGroups][32][kEpiStride]
+  static constexpr int tok_t = epi + kEpiGroups * 32 * kEpiStride * 4;  // int [2][BN] (FINALIZE token tables)
   static constexpr int tok_w = tok_t + 2 * BN * 4;           // float [2][BN]
   static constexpr int bars = tok_w + 2 * BN * 4;            // uint64 [3*kStages + 2*kAccBufs + 1]
   static constexpr int misc = bars + (3 * kStages + 2 * kAccBufs + 1) * 8;  // tmem base, abort flag
@@ -193,27 +202,29 @@ MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, 
 }
 
 // Named barrier 1 over the 128 epilogue threads.
-MOE_DEVINL void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier over the 128 threads of epilogue group g (ids 1 and 3; 2 is the producers').
+MOE_DEVINL void epi_bar(int g) { asm volatile("bar.sync %0, 128;" ::"r"(1 + 2 * g) : "memory"); }
 
-// True on every epilogue thread if `pred` holds on any of them (barrier 1 with an OR reduction).
-MOE_DEVINL bool epi_any(bool pred) {
+// True on every thread of epilogue group g if `pred` holds on any of them
+// (that group's named barrier with an OR reduction).
+MOE_DEVINL bool epi_any(int g, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred pi, po;\n\t"
       "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "bar.red.or.pred po, %2, 128, pi;\n\t"
       "selp.u32 %0, 1, 0, po;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred))
+      : "r"(static_cast<uint32_t>(pred)), "r"(1 + 2 * g)
       : "memory");
   return r != 0;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int EG>
+__global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xt,
                         const GemmParams p) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EG>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -291,13 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int U = unit_start[E];
   const int total_units = U * (MT / MTC);
 
-  if (warp == 0 || warp >= kFirstExtraProducer) {
+  if (warp == 0 || (C::kProducers > 1 && warp >= kExtraWarp)) {
     // ---------------- producers ----------------
     // Stage fill i (counted over this CTA's units and K steps) is issued by
     // producer i % kProducers: bulk copies from one issuing thread are served
     // one after another, so several issuing warps keep more of them in flight
     // (the weight and token tiles of a compute-bound unit are mostly L2 hits).
-    const int pid = warp == 0 ? 0 : warp - kFirstExtraProducer + 1;
+    constexpr int kProducers = C::kProducers;
+    const int pid = warp == 0 ? 0 : warp - kExtraWarp + 1;
     int* s_last = reinterpret_cast<int*>(smem + C::last);  // [kProducers][S] last fill index per stage
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
@@ -431,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int zero = 0;
       mbar_wait_bounded(mma_done, 0, p.timeout_ns, reinterpret_cast<volatile int*>(&zero));
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < kExtraWarp) {
     // ---------------- scale staging warps 6..9 ----------------
     // The block-scaled MMA reads its scales from tensor memory.  Each of these
     // warps (one per TMEM lane quadrant) writes the stage's 32 scale columns
@@ -479,9 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int m = 32 * q + lane;       // weight row of the tile owned by this thread
-    const int et = threadIdx.x - 64;   // 0..127
+    const int eg = warp >= kExtraWarp ? 1 : 0;                          // epilogue group
+    const int et = eg ? threadIdx.x - 32 * kExtraWarp : threadIdx.x - 64;  // 0..127 within the group
+    float* s_epi_g = s_epi + eg * 32 * kEpiStride;
     const float x_scale = __ldg(p.x_scale);
-    if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && et == 0) *p.h_scale_out = p.h_scale;
+    if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && eg == 0 && et == 0)
+      *p.h_scale_out = p.h_scale;
     int acc_i = 0;
     int e_hint = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
@@ -491,11 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         --acc_i;
         continue;
       }
+      if (acc_i % C::kEpiGroups != eg) continue;  // the other group drains this unit
       const int b = acc_i % C::kAccBufs;
       const bool got = mbar_wait_bounded(&acc_full[b], (acc_i / C::kAccBufs) & 1, p.timeout_ns, s_abort);
-      // The four epilogue warps decide together, so none is left waiting on a
+      // The four warps of the group decide together, so none is left waiting on a
       // named barrier that the others have abandoned.
-      if (epi_any(!got)) {
+      if (epi_any(eg, !got)) {
         if (et == 0) {
           if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 4);
           *s_abort = 1;
@@ -519,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok_tab[et] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
           w_tab[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
         }
-        epi_bar();
+        epi_bar(eg);
       }
       for (int j0 = 0; j0 < d.rows; j0 += 32) {
         uint32_t r[32];
@@ -583,11 +599,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // so an NVFP4 block (amax, scale, codes) lives in one thread's registers.
           const int I = N / 2;
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) s_epi[jj * kEpiStride + m] = alpha * __uint_as_float(r[jj]);
-          epi_bar();
+          for (int jj = 0; jj < 32; ++jj) s_epi_g[jj * kEpiStride + m] = alpha * __uint_as_float(r[jj]);
+          epi_bar(eg);
           const int jj = et >> 2, blk = et & 3;
           if (jj < jn) {
-            const float* gp = s_epi + jj * kEpiStride + 16 * blk;
+            const float* gp = s_epi_g + jj * kEpiStride + 16 * blk;
             float h[16];
             float amax = 0.0f;
 #pragma unroll
@@ -613,9 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int t = 0; t < 4; ++t) dst[t] = make_float4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
             }
           }
-          epi_bar();
+          epi_bar(eg);
         }
       }
+      // with two groups, this group's next unit rewrites the same token table
+      if (C::kEpiGroups > 1 && p.epilogue == MOE_EPI_FINALIZE) epi_bar(eg);
       tc_fence_before();
       mbar_arrive(&acc_empty[b]);
     }
@@ -652,22 +670,22 @@ bool make_code_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, int EG>
 moe_status prepare_gemm() {
-  return cudaFuncSetAttribute(grouped_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<BN>::smem_bytes) == cudaSuccess
+  return cudaFuncSetAttribute(grouped_gemm_kernel<BN, EG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<BN, EG>::smem_bytes) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_RESOURCE;
 }
 
-template <int BN>
+template <int BN, int EG>
 moe_status launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_xt, const GemmParams& p, int64_t max_units,
                        cudaStream_t st) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, EG>;
   int grid = num_sms();
   if (grid < 1) return MOE_ERR_CUDA;
   if (max_units < grid) grid = static_cast<int>(max_units);
-  grouped_gemm_kernel<BN><<<grid, kThreads, C::smem_bytes, st>>>(tm_x, tm_xt, p);
+  grouped_gemm_kernel<BN, EG><<<grid, C::kThreads, C::smem_bytes, st>>>(tm_x, tm_xt, p);
   return check_launch();
 }
 
@@ -755,6 +773,7 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   if (!p.err) return MOE_ERR_CUDA;
 
   const int bn = gemm_tile_rows(a_rows_alloc, E);
+  const bool two_groups = bn == 128 && epilogue == MOE_EPI_FINALIZE;
   const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
   if (max_units > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   // routed-row tiles come as 32-row boxes, or as one box when a unit fills the whole tile
@@ -762,7 +781,7 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
   if (!make_code_map(&tm_xt, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, bn)) return MOE_ERR_CUDA;
   {
-    const moe_status ps = bn == 64 ? prepare_gemm<64>() : prepare_gemm<128>();
+    const moe_status ps = bn == 64 ? prepare_gemm<64, 1>() : two_groups ? prepare_gemm<128, 2>() : prepare_gemm<128, 1>();
     if (ps != MOE_OK) return ps;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -770,7 +789,9 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  moe_status s = bn == 64 ? launch_gemm<64>(tm_x, tm_xt, p, max_units, st) : launch_gemm<128>(tm_x, tm_xt, p, max_units, st);
+  moe_status s = bn == 64       ? launch_gemm<64, 1>(tm_x, tm_xt, p, max_units, st)
+                 : two_groups ? launch_gemm<128, 2>(tm_x, tm_xt, p, max_units, st)
+                              : launch_gemm<128, 1>(tm_x, tm_xt, p, max_units, st);
   if (s != MOE_OK) return s;
   if (epilogue == MOE_EPI_FINALIZE) {
     if (p.fin_gather)
