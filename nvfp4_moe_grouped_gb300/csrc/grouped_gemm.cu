@@ -87,17 +87,18 @@ constexpr uint32_t kSfSlotCols = 32;      // 16 columns weight scales + 16 colum
 constexpr int kEpiStride = 130;           // floats per staged routed row (128 tile rows + 2: fewer bank conflicts)
 
 // EG = epilogue warp groups.  With one group, four copy-issuing warps (0,
-// 10-12) keep more bulk copies in flight.  Two groups are for a launch whose
-// epilogue is slower than its mainloop (FINALIZE at 128 routed rows: short
-// K = I units, an atomic per 4 outputs): warps 10-13 form a second group that
-// takes every other unit, so two accumulators drain at once; that launch keeps
-// one copy warp and four stages to fit the second staging buffer.
+// 10-12) keep more bulk copies in flight.  Two groups are for a FINALIZE launch
+// whose epilogue is slower than its mainloop (128 routed rows: short K = I
+// units, an atomic per 4 outputs): warps 10-13 form a second group that takes
+// every other unit, so two accumulators drain at once.  That configuration
+// serves FINALIZE only, which needs no staging tile, and keeps one copy warp.
 template <int BN, int EG>
 struct Cfg {
   static constexpr int kEpiGroups = EG;
   static constexpr int kProducers = EG == 1 ? 4 : 1;
   static constexpr int kThreads = 32 * (kExtraWarp + (kProducers - 1) + 4 * (kEpiGroups - 1));
-  static constexpr int kStages = BN == 64 ? 7 : (EG == 1 ? 5 : 4);
+  static constexpr bool kFinalizeOnly = EG == 2;
+  static constexpr int kStages = BN == 64 ? 7 : 5;
   static constexpr int kXStageBytes = BN * kBK / 2;
   static constexpr uint32_t kAccCols = BN;
   // Accumulator buffers: the epilogue of a unit may lag the mainloop by kAccBufs - 1 units
@@ -114,8 +115,8 @@ struct Cfg {
   static constexpr int w = 0;
   static constexpr int x = w + kStages * kWStageBytes;
   static constexpr int sfx = x + kStages * kXStageBytes;
-  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [kEpiGroups][32][kEpiStride]
-  static constexpr int tok_t = epi + kEpiGroups * 32 * kEpiStride * 4;  // int [2][BN] (FINALIZE token tables)
+  static constexpr int epi = sfx + kStages * kSfStageBytes;  // float [32][kEpiStride] (SiLU staging tile)
+  static constexpr int tok_t = epi + (kFinalizeOnly ? 0 : 32 * kEpiStride * 4);  // int [2][BN] (FINALIZE tables)
   static constexpr int tok_w = tok_t + 2 * BN * 4;           // float [2][BN]
   static constexpr int bars = tok_w + 2 * BN * 4;            // uint64 [3*kStages + 2*kAccBufs + 1]
   static constexpr int misc = bars + (3 * kStages + 2 * kAccBufs + 1) * 8;  // tmem base, abort flag
@@ -248,6 +249,10 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, N = p.N, K = p.K;
+  if (C::kFinalizeOnly && p.epilogue != MOE_EPI_FINALIZE) {  // the host never launches this; no smem tile for it
+    if (threadIdx.x == 0) record_error(p.err, MOE_ERR_INVALID_ARG, 9);
+    return;
+  }
   const int MT = N / kBM;
   const int MTC = p.mt_chunk;
   const int KT = (K + kBK - 1) / kBK;
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     const int m = 32 * q + lane;       // weight row of the tile owned by this thread
     const int eg = warp >= kExtraWarp ? 1 : 0;                          // epilogue group
     const int et = eg ? threadIdx.x - 32 * kExtraWarp : threadIdx.x - 64;  // 0..127 within the group
-    float* s_epi_g = s_epi + eg * 32 * kEpiStride;
+    float* s_epi_g = s_epi;  // only the one-group configuration stages tiles (SiLU)
     const float x_scale = __ldg(p.x_scale);
     if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && eg == 0 && et == 0)
       *p.h_scale_out = p.h_scale;
@@ -773,6 +778,8 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
   if (!p.err) return MOE_ERR_CUDA;
 
   const int bn = gemm_tile_rows(a_rows_alloc, E);
+  // two epilogue groups pay off where FINALIZE outlasts the mainloop (128-row tiles); at decode the
+  // weight stream dominates and four copy warps are worth more (measured: 0.303 vs 0.319 ms, C4 down)
   const bool two_groups = bn == 128 && epilogue == MOE_EPI_FINALIZE;
   const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
   if (max_units > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
