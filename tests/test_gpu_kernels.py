@@ -204,6 +204,26 @@ def test_grouped_gemm_none_matches_oracle(counts, N, K):
     tol_check(bf16_to_np(out)[dst], ref, "grouped GEMM NONE")
 
 
+def test_grouped_gemm_none_max_experts():
+    """E = 1024 (the largest expert count a launch takes), 0-3 rows per expert, one partial K stage."""
+    rng = np.random.default_rng(1024)
+    counts = rng.integers(0, 4, 1024).tolist()
+    E, N, K = 1024, 128, 64
+    offs = counts_to_offsets(counts)
+    R = int(offs[-1])
+    x = inputs.activations(R, K, seed=5)
+    xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
+    w = inputs.expert_weights(E, N, K, 700)
+    wq = oracle.quantize_weights(w.numpy())
+    ref = oracle.grouped_gemm(xc, xs, xsc, *wq, offs, N, K)
+    codes, sf, s, dst = _routed_operand(x, offs.astype(np.int64))
+    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=False)
+    out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV), moe.EPI_NONE)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    tol_check(bf16_to_np(out)[dst], ref, "E=1024")
+
+
 def test_grouped_gemm_identity_expert_is_exact():
     """W = identity (e2m1 1.0, scales 1), inputs on the e2m1 grid: the output is the input, exactly."""
     K = N = 256
@@ -376,7 +396,12 @@ def _layer_case(T, E, k, H, I, zipf=None):
 
 
 @pytest.mark.parametrize("T,E,k,H,I,zipf", [(16, 8, 2, 256, 128, None), (96, 64, 6, 512, 192, None),
-                                            (128, 32, 4, 256, 128, 1.1)])
+                                            (128, 32, 4, 256, 128, 1.1),
+                                            # degenerate shapes: one token and one expert; every expert
+                                            # selected (k = E); one token over mostly empty experts with a
+                                            # single partial K stage in the down GEMM (I = 64)
+                                            (1, 1, 1, 256, 128, None), (40, 4, 4, 256, 128, None),
+                                            (1, 256, 8, 256, 64, None), (33, 3, 2, 384, 64, None)])
 def test_moe_forward_matches_oracle(T, E, k, H, I, zipf):
     x, logits, w13f, w2f = _layer_case(T, E, k, H, I, zipf)
     w13 = oracle.quantize_weights(w13f.numpy())
