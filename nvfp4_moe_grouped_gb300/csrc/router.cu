@@ -161,10 +161,11 @@ RouterShape router_shape(int T, int E, int H) {
   s.NE = (E + 15) / 16 * 16;
   s.KB = H / kRBK;
   const int sms = num_sms() > 0 ? num_sms() : 148;
-  // about one CTA per SM; more splits would add partial-tile traffic (128 x NE floats each) for little gain
+  // up to one CTA per SM, but at most 8 splits: each split adds T x E floats of partial sums that the
+  // routing kernel reads back per token
   int splits = (sms + s.tiles - 1) / s.tiles;
   if (splits > s.KB) splits = s.KB;
-  if (splits > 32) splits = 32;
+  if (splits > 8) splits = 8;
   if (splits < 1) splits = 1;
   s.splits = splits;
   s.part_bytes = (static_cast<size_t>(s.tiles) * splits * 128 * s.NE * sizeof(float) + 255) / 256 * 256;
