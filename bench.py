@@ -177,6 +177,24 @@ class ClockSampler:
                 "samples": len(sm), "window": window}
 
 
+# ------------------------------------------------------------------ replicas (N > 1)
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (x itself with one rank): the job's time is its slowest replica's."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    if torch.distributed.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank in (at most) ms."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ setup
 
 def make_layer(T, E, k, H, I, zipf, dev):
@@ -482,12 +500,9 @@ def run_ours(args, rank, world, local_rank):
     graph_st.launch()
     torch.cuda.synchronize()
     graph_last_stages = graph_st.stage_ms()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_step = ms / args.steps
-    value = world * T / (ms_step / 1e3)
+    value = whole_job_rate(T, world, ms_step)
 
     # ---- end to end through moe_forward with pinned host buffers
     # Every step copies its inputs from pinned host memory and reads its output back.  The copies of one
@@ -542,11 +557,8 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * T * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = whole_job_rate(T * args.steps, world, e2e_ms)
     # the output read back is the layer's output for these inputs (the device-timed graph computed it too;
     # FINALIZE's atomics may order the FP32 sums differently, so compare by relative difference)
     ref_out = out_g.float().cpu()
