@@ -191,6 +191,11 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
  *   w_gate   bf16 [E][H], 16-byte aligned
  *   logits   f32 [T][E] out, or NULL (not written: the routing kernel adds
  *            the partial sums as it reads them)
+ *   x_scale  f32 [1] out, or NULL: the NVFP4 decode multiplier of x,
+ *            s = max|x| / (6*448) (1 when x is all zero), with max|x| taken
+ *            by the logits GEMM from the x tiles it loads anyway -- what
+ *            nvfp4_quantize would compute as its dynamic scale, so a caller
+ *            can quantise x with that static scale and skip its amax pass
  *   topk_id ... expanded_to_row   as moe_route_permute
  *   ws / ws_bytes  workspace of moe_router_workspace_size(T, E, H, k) bytes,
  *                  queried with the device that will run the call current
@@ -198,9 +203,9 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
  * ------------------------------------------------------------------------- */
 MOE_API size_t moe_router_workspace_size(int T, int E, int H, int k);
 MOE_API moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int T, int E, int H, int k, float* logits,
-                              int32_t* topk_id, float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
-                              int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws, size_t ws_bytes,
-                              void* stream);
+                              float* x_scale, int32_t* topk_id, float* topk_w, int32_t* expert_offsets,
+                              int32_t* perm_to_expanded, int32_t* expanded_to_perm, int32_t* expanded_to_row,
+                              void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * nvfp4_quantize -- NVFP4 quantisation of rows of a bf16 or f32 matrix.
@@ -364,6 +369,21 @@ MOE_API size_t moe_forward_workspace_size(int T, int E, int k, int H, int I);
 MOE_API moe_status moe_forward_workspace_layout(int T, int E, int k, int H, int I, moe_forward_layout* layout);
 MOE_API moe_status moe_forward(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k, int H,
                        int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_forward_gated -- moe_forward with the router in front: the logits come
+ * from moe_router (x . w_gate^T on the tensor cores), and the activation
+ * quantiser takes x's decode multiplier from the router's logits GEMM, which
+ * reads every element of x anyway, instead of a separate amax pass.
+ * Same arguments as moe_forward with w_gate (bf16 [E][H], device, 16-byte
+ * aligned) in place of the logits; requires E <= 256; ws_bytes >=
+ * moe_forward_gated_workspace_size(...), whose first
+ * moe_forward_workspace_size(...) bytes follow moe_forward_workspace_layout.
+ * ------------------------------------------------------------------------- */
+MOE_API size_t moe_forward_gated_workspace_size(int T, int E, int k, int H, int I);
+MOE_API moe_status moe_forward_gated(const uint16_t* x, const uint16_t* w_gate, const moe_weights* w, int T, int E,
+                                     int k, int H, int I, float h_scale, uint16_t* out, void* ws, size_t ws_bytes,
+                                     void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_forward_graph_* -- the whole layer as one CUDA graph.

@@ -120,11 +120,12 @@ def moe_route_permute(logits: torch.Tensor, k: int, stream=None) -> Routing:
 
 
 def moe_router(x: torch.Tensor, w_gate: torch.Tensor, k: int, want_logits: bool = True, stream=None,
-               out: Routing | None = None, logits: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+               out: Routing | None = None, logits: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+               x_scale: torch.Tensor | None = None):
     """Router logits x . w_gate^T on the tensor cores (bf16 in, FP32 sums), then moe_route_permute.
 
-    `out`, `logits` and `ws` may be given preallocated (e.g. for graph capture).
-    Returns (Routing, logits f32 [T][E] or None)."""
+    `out`, `logits` and `ws` may be given preallocated (e.g. for graph capture); `x_scale` (f32 [1]),
+    when given, receives x's NVFP4 decode multiplier.  Returns (Routing, logits f32 [T][E] or None)."""
     if x.dtype != torch.bfloat16 or w_gate.dtype != torch.bfloat16:
         raise TypeError("x and w_gate must be bf16")
     x = x.contiguous()
@@ -145,7 +146,8 @@ def moe_router(x: torch.Tensor, w_gate: torch.Tensor, k: int, want_logits: bool 
     elif ws.numel() < wsb:
         raise ValueError("router workspace too small")
     _check("moe_router", L.moe_router(
-        _ptr(x), _ptr(w_gate), T, E, H, k, _ptr(logits), _ptr(r.topk_id), _ptr(r.topk_w), _ptr(r.expert_offsets),
+        _ptr(x), _ptr(w_gate), T, E, H, k, _ptr(logits), _ptr(x_scale), _ptr(r.topk_id), _ptr(r.topk_w),
+        _ptr(r.expert_offsets),
         _ptr(r.perm_to_expanded), _ptr(r.expanded_to_perm), _ptr(r.expanded_to_row), _ptr(ws), wsb,
         _stream(stream)))
     return r, logits
@@ -298,12 +300,26 @@ def moe_finalize(y: torch.Tensor, topk_w: torch.Tensor, row_of_item: torch.Tenso
 class MoeForward:
     """A reusable workspace for moe_forward at one (T, E, k, H, I)."""
 
-    def __init__(self, T: int, E: int, k: int, H: int, I: int, device="cuda"):
+    def __init__(self, T: int, E: int, k: int, H: int, I: int, device="cuda", gated: bool = False):
         self.T, self.E, self.k, self.H, self.I = T, E, k, H, I
         L = _L()
         self.layout = ForwardLayout()
         _check("moe_forward_workspace_layout", L.moe_forward_workspace_layout(T, E, k, H, I, ctypes.byref(self.layout)))
-        self.ws = torch.zeros(self.layout.total, dtype=torch.uint8, device=device)
+        # moe_forward_gated needs the router's workspace after moe_forward's (same layout up front)
+        total = L.moe_forward_gated_workspace_size(T, E, k, H, I) if gated else self.layout.total
+        if gated and total == 0:
+            raise MoeError("moe_forward_gated_workspace_size", 1)
+        self.ws = torch.zeros(total, dtype=torch.uint8, device=device)
+
+    def gated(self, x, w_gate, w13: PreparedWeights, w2: PreparedWeights, h_scale: float, out=None, stream=None):
+        """moe_forward_gated: the router (x . w_gate^T, top-k, permutation) in front of the layer."""
+        if out is None:
+            out = _empty((self.T, self.H), torch.bfloat16, x.device)
+        wts = Weights(_ptr(w13.blocked), _ptr(w13.scale), _ptr(w2.blocked), _ptr(w2.scale))
+        _check("moe_forward_gated", _L().moe_forward_gated(
+            _ptr(x), _ptr(w_gate), ctypes.byref(wts), self.T, self.E, self.k, self.H, self.I, float(h_scale),
+            _ptr(out), _ptr(self.ws), self.ws.numel(), _stream(stream)))
+        return out
 
     def view(self, name: str, dtype, shape):
         off = getattr(self.layout, name)

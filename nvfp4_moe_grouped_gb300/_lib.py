@@ -59,7 +59,7 @@ SIGNATURES = {
     "moe_route_permute_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_route_permute": (c_int, [c_void_p, c_int, c_int, c_int] + [c_void_p] * 7 + [c_size_t, c_void_p]),
     "moe_router_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
-    "moe_router": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int] + [c_void_p] * 8 + [c_size_t, c_void_p]),
+    "moe_router": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int] + [c_void_p] * 9 + [c_size_t, c_void_p]),
     "moe_route_permute_static_scratch_bytes": (c_size_t, []),
     "moe_route_permute_static": (c_int, [c_void_p, c_int, c_int, c_int] + [c_void_p] * 7),
     "nvfp4_quantize_workspace_size": (c_size_t, [c_int]),
@@ -71,6 +71,9 @@ SIGNATURES = {
     "moe_finalize": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "moe_fp4_mma_probe": (c_int, [c_int, c_int, c_void_p, c_void_p]),
     "moe_forward_workspace_size": (c_size_t, [c_int] * 5),
+    "moe_forward_gated_workspace_size": (c_size_t, [c_int] * 5),
+    "moe_forward_gated": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,
+                                  c_void_p, c_size_t, c_void_p]),
     "moe_forward_workspace_layout": (c_int, [c_int] * 5 + [c_void_p]),
     "moe_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,
                             c_void_p, c_size_t, c_void_p]),

@@ -50,6 +50,14 @@ extern "C" size_t moe_forward_workspace_size(int T, int E, int k, int H, int I) 
   return L.total;
 }
 
+// moe_forward_gated: moe_forward's workspace, then the router's.
+extern "C" size_t moe_forward_gated_workspace_size(int T, int E, int k, int H, int I) {
+  const size_t base = moe_forward_workspace_size(T, E, k, H, I);
+  const size_t rws = moe_router_workspace_size(T, E, H, k);
+  if (base == 0 || rws == 0) return 0;
+  return base + align256(rws);
+}
+
 namespace {
 
 // Checks everything the stage calls would check, so moe_forward either fails
@@ -71,10 +79,13 @@ moe_status forward_check(const uint16_t* x, const float* logits, const moe_weigh
 }
 
 // The layer's four stages; when `ev` is given, ev[i] is recorded (as an external
-// event, visible to timing even inside a captured graph) after stage i.
-moe_status forward_stages(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k, int H,
-                          int I, float h_scale, uint16_t* out, void* ws, const moe_forward_layout& L,
-                          cudaStream_t stream, cudaEvent_t* ev, bool external) {
+// event, visible to timing even inside a captured graph) after stage i.  With
+// `w_gate` the first stage is moe_router (logits GEMM, routing, and x's decode
+// multiplier from the GEMM's own pass over x) and the quantiser takes that
+// multiplier as a static scale; otherwise the logits are an input.
+moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t* w_gate, const moe_weights* w,
+                          int T, int E, int k, int H, int I, float h_scale, uint16_t* out, void* ws,
+                          const moe_forward_layout& L, cudaStream_t stream, cudaEvent_t* ev, bool external) {
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
   auto mark = [&](int i) -> moe_status {
@@ -98,11 +109,16 @@ moe_status forward_stages(const uint16_t* x, const float* logits, const moe_weig
   uint8_t* h_sf = static_cast<uint8_t*>(at(L.h_sf));
   moe_status s = mark(0);
   if (s != MOE_OK) return s;
-  s = moe_route_permute(logits, T, E, k, topk_id, topk_w, offs, p2e, e2p, e2r, at(L.route_ws),
-                        moe_route_permute_workspace_size(T, E, k), stream);
+  if (w_gate) {
+    s = moe_router(x, w_gate, T, E, H, k, nullptr, x_scale, topk_id, topk_w, offs, p2e, e2p, e2r, at(L.total),
+                   moe_router_workspace_size(T, E, H, k), stream);
+  } else {
+    s = moe_route_permute(logits, T, E, k, topk_id, topk_w, offs, p2e, e2p, e2r, at(L.route_ws),
+                          moe_route_permute_workspace_size(T, E, k), stream);
+  }
   if (s != MOE_OK || (s = mark(1)) != MOE_OK) return s;
-  s = nvfp4_quantize(x, MOE_IN_BF16, T, H, 1, x_scale, 1, R, k, e2r, x_codes, x_sf, MOE_SF_TILED, L.padded_rows,
-                     at(L.quant_ws), nvfp4_quantize_workspace_size(1), stream);
+  s = nvfp4_quantize(x, MOE_IN_BF16, T, H, 1, x_scale, w_gate ? 0 : 1, R, k, e2r, x_codes, x_sf, MOE_SF_TILED,
+                     L.padded_rows, at(L.quant_ws), nvfp4_quantize_workspace_size(1), stream);
   if (s != MOE_OK || (s = mark(2)) != MOE_OK) return s;
   moe_epilogue_args ep{};
   ep.h_scale = h_scale;
@@ -132,8 +148,24 @@ extern "C" moe_status moe_forward(const uint16_t* x, const float* logits, const 
   moe_forward_layout L;
   moe_status s = forward_check(x, logits, w, T, E, k, H, I, h_scale, out, ws, ws_bytes, &L);
   if (s != MOE_OK) return s;
-  return forward_stages(x, logits, w, T, E, k, H, I, h_scale, out, ws, L, static_cast<cudaStream_t>(stream), nullptr,
-                        false);
+  return forward_stages(x, logits, nullptr, w, T, E, k, H, I, h_scale, out, ws, L, static_cast<cudaStream_t>(stream),
+                        nullptr, false);
+}
+
+extern "C" moe_status moe_forward_gated(const uint16_t* x, const uint16_t* w_gate, const moe_weights* w, int T,
+                                        int E, int k, int H, int I, float h_scale, uint16_t* out, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (!w_gate) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate)) return MOE_ERR_MISALIGNED;
+  if (E > 256) return MOE_ERR_UNSUPPORTED;
+  moe_forward_layout L;
+  // forward_check validates everything but the logits, which this call computes
+  moe_status s = forward_check(x, reinterpret_cast<const float*>(w_gate), w, T, E, k, H, I, h_scale, out, ws, ws_bytes,
+                               &L);
+  if (s != MOE_OK) return s;
+  if (ws_bytes < moe_forward_gated_workspace_size(T, E, k, H, I)) return MOE_ERR_WORKSPACE;
+  return forward_stages(x, nullptr, w_gate, w, T, E, k, H, I, h_scale, out, ws, L, static_cast<cudaStream_t>(stream),
+                        nullptr, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -180,11 +212,11 @@ extern "C" moe_status moe_forward_graph_create(const uint16_t* x, const float* l
       if (cudaEventCreate(&e) != cudaSuccess) return fail(MOE_ERR_CUDA);
   // One eager pass first: every host-side preparation (kernel attributes, cached
   // device addresses) happens outside the capture.
-  s = forward_stages(x, logits, w, T, E, k, H, I, h_scale, out, ws, L, st, nullptr, false);
+  s = forward_stages(x, logits, nullptr, w, T, E, k, H, I, h_scale, out, ws, L, st, nullptr, false);
   if (s != MOE_OK) return fail(s);
   if (cudaStreamSynchronize(st) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return fail(MOE_ERR_CUDA);
-  s = forward_stages(x, logits, w, T, E, k, H, I, h_scale, out, ws, L, st, g->timed ? g->ev : nullptr, true);
+  s = forward_stages(x, logits, nullptr, w, T, E, k, H, I, h_scale, out, ws, L, st, g->timed ? g->ev : nullptr, true);
   cudaError_t ce = cudaStreamEndCapture(st, &raw);
   if (s != MOE_OK) return fail(s);
   if (ce != cudaSuccess || !raw) return fail(MOE_ERR_CUDA);

@@ -45,6 +45,8 @@ struct PartialLogits {
   const float* part;  // [tiles][splits][128][NE]
   int splits, NE;
   float* logits_out;  // optional copy of the summed logits, [T][E]
+  const uint32_t* x_amax_bits;  // optional: max |x| as an f32 bit pattern ...
+  float* x_scale;               // ... turned into x's NVFP4 decode multiplier here
 };
 
 template <int NV, bool PARTS>  // NV: logits per lane, NV * 32 >= E; PARTS: read partial sums
@@ -55,6 +57,10 @@ __global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __rest
                                                               PartialLogits pl) {
   extern __shared__ int hist[];  // [E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (PARTS && pl.x_scale && blockIdx.x == 0 && threadIdx.x == 0) {
+    const float a = __uint_as_float(*pl.x_amax_bits);
+    *pl.x_scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);  // s = amax / (6 * 448), 1 when amax = 0
+  }
   const int t0 = blockIdx.x * d.chunk_tokens;
   const int t1 = min(d.T, t0 + d.chunk_tokens);
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) hist[e] = 0;
@@ -263,15 +269,15 @@ namespace moe {
 // Routing and permutation from full logits, or (part != nullptr) from the
 // router GEMM's partial sums.  Arguments are validated by the callers.
 moe_status route_permute_enqueue(const float* logits, const float* part, int splits, int NE, float* logits_out,
-                                 int T, int E, int k, int32_t* topk_id, float* topk_w, int32_t* expert_offsets,
-                                 int32_t* perm_to_expanded, int32_t* expanded_to_perm, int32_t* expanded_to_row,
-                                 void* ws, cudaStream_t st) {
+                                 const uint32_t* x_amax_bits, float* x_scale, int T, int E, int k, int32_t* topk_id,
+                                 float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
+                                 int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws, cudaStream_t st) {
   RouteDims d = route_dims(T, E, k);
   int32_t* counts = static_cast<int32_t*>(ws);
   int32_t* pads = route_pad_offsets(ws, T, E, k);
   const size_t hist_bytes = sizeof(int) * E;
   const int nv = (E + 31) / 32;
-  const PartialLogits pl{part, splits, NE, logits_out};
+  const PartialLogits pl{part, splits, NE, logits_out, x_amax_bits, x_scale};
 #define MOE_ROUTE(NV)                                                                                         \
   (part ? route_kernel<NV, true><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl) \
         : route_kernel<NV, false><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl))
@@ -300,7 +306,7 @@ extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k
   if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < moe_route_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
-  return route_permute_enqueue(logits, nullptr, 0, 0, nullptr, T, E, k, topk_id, topk_w, expert_offsets,
-                               perm_to_expanded, expanded_to_perm, expanded_to_row, ws,
+  return route_permute_enqueue(logits, nullptr, 0, 0, nullptr, nullptr, nullptr, T, E, k, topk_id, topk_w,
+                               expert_offsets, perm_to_expanded, expanded_to_perm, expanded_to_row, ws,
                                static_cast<cudaStream_t>(stream));
 }

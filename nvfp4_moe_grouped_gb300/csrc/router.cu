@@ -14,16 +14,18 @@
 // share of H with tcgen05.mma kind::f16 (M = 128 tokens, N = E rounded up to 16,
 // K = 16, FP32 accumulator in tensor memory) and stores its FP32 partial tile.
 // The routing kernel adds the partials in split order (deterministic) as it
-// reads each token's logits, so the logits never make a round trip of their own.  Roles in the GEMM CTA: lane 0 of warp 0 issues the TMA loads (128-
-// byte swizzle, rows past T or E read as zeros), lane 0 of warp 1 the MMAs; all
-// four warps then drain the accumulator.  Every wait is bounded.
+// reads each token's logits, so the logits never make a round trip of their
+// own.  Roles in the GEMM CTA: lane 0 of warp 0 issues the TMA loads (128-byte
+// swizzle, rows past T or E read as zeros), lane 0 of warp 1 the MMAs, warp 2
+// (when asked) takes max |x| over the x tiles for the activation quantiser;
+// all four warps then drain the accumulator.  Every wait is bounded.
 #include "common.cuh"
 
 namespace moe {
 moe_status route_permute_enqueue(const float* logits, const float* part, int splits, int NE, float* logits_out,
-                                 int T, int E, int k, int32_t* topk_id, float* topk_w, int32_t* expert_offsets,
-                                 int32_t* perm_to_expanded, int32_t* expanded_to_perm, int32_t* expanded_to_row,
-                                 void* ws, cudaStream_t st);
+                                 const uint32_t* x_amax_bits, float* x_scale, int T, int E, int k, int32_t* topk_id,
+                                 float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
+                                 int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws, cudaStream_t st);
 namespace {
 
 constexpr int kRThreads = 128;
@@ -36,7 +38,8 @@ constexpr uint32_t kRTmemCols = 256;
 
 struct RouterParams {
   int T, E, NE, KB, splits;
-  float* part;  // [tiles][splits][128][NE]
+  float* part;           // [tiles][splits][128][NE]
+  uint32_t* amax_bits;   // optional: max |x| (bit pattern), for the activation quantiser
   int32_t* err;
   uint64_t timeout_ns;
 };
@@ -61,8 +64,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int nk = kb1 - kb0;  // >= 1: splits <= KB
   const uint32_t b_bytes = static_cast<uint32_t>(p.NE) * 128;
 
+  const bool amax_on = p.amax_bits != nullptr;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    // a stage is free once the MMAs and (when x's amax is wanted) warp 2 are done with it
+    for (int s = 0; s < kRStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], amax_on ? 2 : 1); }
     mbar_init(acc_full, 1);
     *s_abort = 0;
     fence_barrier_init();
@@ -118,6 +123,35 @@ __global__ void __launch_bounds__(kRThreads, 1)
       mma_commit(&empty[s]);
     }
     mma_commit(acc_full);  // arrives once every MMA issued above has completed
+  } else if (warp == 2 && amax_on) {
+    // ---- max |x| over this CTA's x tiles (each x element is in exactly one CTA's tiles; rows past T
+    // are zero-filled), for the NVFP4 decode multiplier of the activation quantiser ----
+    uint32_t m = 0;  // max of |bf16| bit patterns: the order of non-negative values
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kRStages;
+      const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
+      const bool got = mbar_wait_bounded(&full[s], ph, p.timeout_ns, s_abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 33);
+          *s_abort = 1;
+        }
+        break;
+      }
+      const uint4* a4 = reinterpret_cast<const uint4*>(s_a + s * kRAStage);
+#pragma unroll 4
+      for (int j = lane; j < kRAStage / 16; j += 32) {
+        const uint4 u = a4[j];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0 && m > 0) atomicMax(p.amax_bits, m << 16);  // the bf16 pattern as an f32 pattern
   }
   __syncwarp();
 
@@ -193,13 +227,13 @@ using namespace moe;
 extern "C" size_t moe_router_workspace_size(int T, int E, int H, int k) {
   if (T < 1 || E < 1 || H < kRBK || k < 1) return 0;
   const RouterShape s = router_shape(T, E, H);
-  return s.part_bytes + moe_route_permute_workspace_size(T, E, k);
+  return s.part_bytes + 256 + moe_route_permute_workspace_size(T, E, k);  // 256: the amax word
 }
 
 extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int T, int E, int H, int k,
-                                 float* logits, int32_t* topk_id, float* topk_w, int32_t* expert_offsets,
-                                 int32_t* perm_to_expanded, int32_t* expanded_to_perm, int32_t* expanded_to_row,
-                                 void* ws, size_t ws_bytes, void* stream) {
+                                 float* logits, float* x_scale, int32_t* topk_id, float* topk_w,
+                                 int32_t* expert_offsets, int32_t* perm_to_expanded, int32_t* expanded_to_perm,
+                                 int32_t* expanded_to_row, void* ws, size_t ws_bytes, void* stream) {
   if (!x || !w_gate || !topk_id || !topk_w || !expert_offsets || !perm_to_expanded || !expanded_to_perm ||
       !expanded_to_row)
     return MOE_ERR_INVALID_ARG;
@@ -211,7 +245,8 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   const RouterShape s = router_shape(T, E, H);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   float* part = reinterpret_cast<float*>(w8);
-  void* route_ws = w8 + s.part_bytes;
+  uint32_t* amax_bits = reinterpret_cast<uint32_t*>(w8 + s.part_bytes);
+  void* route_ws = w8 + s.part_bytes + 256;
 
   RouterParams p{};
   p.T = T;
@@ -220,6 +255,7 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   p.KB = s.KB;
   p.splits = s.splits;
   p.part = part;
+  p.amax_bits = x_scale ? amax_bits : nullptr;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
   if (!p.err) return MOE_ERR_CUDA;
@@ -230,10 +266,12 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   if (cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem) != cudaSuccess)
     return MOE_ERR_RESOURCE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (x_scale && cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
   router_gemm_kernel<<<dim3(s.tiles, s.splits), kRThreads, kRSmem, st>>>(tm_x, tm_w, p);
   moe_status rs = check_launch();
   if (rs != MOE_OK) return rs;
   // the routing kernel adds the partial sums (in split order) as it reads each token's logits
-  return route_permute_enqueue(nullptr, part, s.splits, s.NE, logits, T, E, k, topk_id, topk_w, expert_offsets,
-                               perm_to_expanded, expanded_to_perm, expanded_to_row, route_ws, st);
+  return route_permute_enqueue(nullptr, part, s.splits, s.NE, logits, x_scale ? amax_bits : nullptr, x_scale, T, E,
+                               k, topk_id, topk_w, expert_offsets, perm_to_expanded, expanded_to_perm,
+                               expanded_to_row, route_ws, st);
 }

@@ -138,10 +138,13 @@ def test_router_matches_oracle(T, E, k, H):
     oracle's routing of the GPU's logits, and agrees with the oracle's own logits except at near-ties."""
     x = inputs.activations(T, H, seed=T)
     wg = inputs.router_gate(E, H)
-    r, lg = moe.moe_router(x.to(DEV), wg.to(DEV), k)
+    xs = torch.zeros(1, dtype=torch.float32, device=DEV)
+    r, lg = moe.moe_router(x.to(DEV), wg.to(DEV), k, x_scale=xs)
     torch.cuda.synchronize()
     assert moe.device_error() == (0, 0)
     xf, wf = x.float().numpy(), wg.float().numpy()
+    # x's NVFP4 decode multiplier, from the GEMM's pass over x: exactly the oracle's
+    assert np.float32(oracle.tensor_scale_from_amax(oracle.amax(xf))) == xs.item()
     ref = oracle.router_logits(xf, wf)
     got = lg.cpu().numpy()
     bound = 4.0 * H * 2.0 ** -24 * (np.abs(xf).astype(np.float64) @ np.abs(wf).astype(np.float64).T)
@@ -414,6 +417,10 @@ def test_moe_forward_matches_oracle(T, E, k, H, I, zipf):
     out = fwd(x.to(DEV), logits.to(DEV), pw13, pw2, h_scale)
     torch.cuda.synchronize()
     assert moe.device_error() == (0, 0)
+    _check_layer(fwd, out, ref, h_scale, T, E, k, H, I)
+
+
+def _check_layer(fwd, out, ref, h_scale, T, E, k, H, I):
     R = T * k
     # routing, permutation and the quantised activations: bit-exact
     assert np.array_equal(fwd.view("topk_id", torch.int32, (T, k)).cpu().numpy(), ref.topk_id)
@@ -436,6 +443,30 @@ def test_moe_forward_matches_oracle(T, E, k, H, I, zipf):
     assert rel < 1e-2, rel
     if not flips.any():
         tol_check(got, ref.out, "moe_forward")
+
+
+@pytest.mark.parametrize("T,E,k,H,I", [(16, 8, 2, 256, 128), (300, 64, 6, 512, 192), (129, 40, 4, 256, 128)])
+def test_moe_forward_gated_matches_oracle(T, E, k, H, I):
+    """The router in front of the layer: the oracle's layer on the GPU router's logits (the logits themselves
+    are checked against the oracle's FP64 sums in test_router_matches_oracle), x's decode multiplier from
+    the router's GEMM, everything else as moe_forward."""
+    x, _, w13f, w2f = _layer_case(T, E, k, H, I)
+    wg = inputs.router_gate(E, H)
+    _, lg = moe.moe_router(x.to(DEV), wg.to(DEV), k)
+    logits = lg.cpu().numpy()
+    w13 = oracle.quantize_weights(w13f.numpy())
+    w2 = oracle.quantize_weights(w2f.numpy())
+    ref = oracle.moe_layer(x.float().numpy(), logits, w13, w2, k)
+    h_scale = float(oracle.tensor_scale_from_amax(oracle.amax(ref.h.astype(np.float32))))
+    pw13 = moe.prepare_expert_weights(w13f.to(DEV), gate_up=True)
+    pw2 = moe.prepare_expert_weights(w2f.to(DEV), gate_up=False)
+    fwd = moe.MoeForward(T, E, k, H, I, gated=True)
+    out = fwd.gated(x.to(DEV), wg.to(DEV), pw13, pw2, h_scale)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    assert np.float32(oracle.tensor_scale_from_amax(oracle.amax(x.float().numpy()))) == \
+        fwd.view("x_scale", torch.float32, (1,)).item()
+    _check_layer(fwd, out, ref, h_scale, T, E, k, H, I)
 
 
 def test_timeout_path_reports_and_recovers():
