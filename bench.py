@@ -58,6 +58,9 @@ def parse():
                          "K=6144, N=2048, NONE epilogue; dense: one dense NVFP4 GEMM M=N=K=--dense-size; "
                          "router: the router logits GEMM + routing for --tokens tokens")
     ap.add_argument("--dense-size", type=int, default=16384)
+    ap.add_argument("--gated", action="store_true",
+                    help="layer workload with the router in front (moe_forward_gated: x and a bf16 gate "
+                         "matrix instead of logits)")
     ap.add_argument("--profile-steps", action="store_true",
                     help="no JSON; only the steps run between cudaProfilerStart/Stop (for ncu)")
     return ap.parse_args()
@@ -773,6 +776,76 @@ def run_dense(args, rank, world, local_rank):
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 
+def run_gated(args, rank, world, local_rank):
+    """The layer with the router in front (moe_forward_gated), as one CUDA graph, beside the same layer fed
+    precomputed logits."""
+    import nvfp4_moe_grouped_gb300 as moe
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T, E, k, H, I = args.tokens, args.experts, args.top_k, args.hidden, args.intermediate
+    x, logits, pw13, pw2 = make_layer(T, E, k, H, I, args.zipf, dev)
+    xd, ld = x.to(dev), logits.to(dev)
+    wg = inputs.router_gate(E, H, device=dev)
+    fwd = moe.MoeForward(T, E, k, H, I, dev, gated=True)
+    h_scale = calibrate_h_scale(moe.MoeForward(T, E, k, H, I, dev), xd, ld, pw13)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(1, args.warmup)):
+        fwd.gated(xd, wg, pw13, pw2, h_scale, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd.gated(xd, wg, pw13, pw2, h_scale, out=out, stream=torch.cuda.current_stream())
+    plain = fwd.graph(xd, ld, pw13, pw2, h_scale, out=torch.empty_like(out), stage_events=False)
+    for _ in range(max(1, args.warmup)):
+        g.replay()
+        plain.launch()
+    torch.cuda.synchronize()
+    weight_bytes = E * (2 * I * H + H * I) * 9 // 16
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if weight_bytes < (256 << 20) else None
+
+    def timed(launch):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            if flush is not None:
+                flush.fill_(1)
+            a.record(stream)
+            launch()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / args.steps
+
+    with ClockSampler(local_rank) as clk:
+        clk.start()
+        ms = timed(g.replay)
+        clk.stop()
+    ms_plain = timed(plain.launch)
+    ms = max_over_ranks(ms, dev)
+    counts = np.diff(fwd.view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy())
+    ab = algorithmic_bytes(counts, T, E, k, H, I)
+    layer_bytes = ab["layer"] - T * E * 4 + E * H * 2   # the gate matrix is read instead of the logits
+    hbm_peak, _, peak_kind = peaks()
+    gbs = layer_bytes / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": whole_job_rate(T, world, ms), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e2m1xe2m1->f32 (router bf16xbf16->f32)",
+            "data": "synthetic",
+            "config": {"workload": f"moe_layer_gated_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf
+                                                                                  else "_uniform"),
+                       "l2": "weights exceed L2; no flush" if flush is None else "256 MB written between steps"},
+            "roofline": {"bound": "hbm", "kernel": "whole layer with the router (one CUDA graph)", "achieved": gbs,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                         "traffic": None, "algorithmic_bytes_per_launch": layer_bytes, "launch_ms": ms},
+            "same_layer_fed_logits_ms": ms_plain,
+            # router GEMM, routing (3), quantiser, gate_up, down, FP32->BF16 per step
+            "gpu_launches": 8 * args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def run_router(args, rank, world, local_rank):
     """The router: logits GEMM x . w_gate^T (bf16, tcgen05) + top-k routing and permutation."""
     import nvfp4_moe_grouped_gb300 as moe
@@ -848,7 +921,9 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     try:
-        if args.workload == "gemm":
+        if args.workload == "layer" and args.gated:
+            run_gated(args, rank, world, local_rank)
+        elif args.workload == "gemm":
             run_gemm(args, rank, world, local_rank)
         elif args.workload == "dense":
             run_dense(args, rank, world, local_rank)
