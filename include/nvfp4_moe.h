@@ -97,7 +97,8 @@ enum { MOE_EPI_NONE = 0, MOE_EPI_SILU_MUL_QUANT = 1, MOE_EPI_FINALIZE = 2 };
 /* Human-readable name of a status code (static string). */
 MOE_API const char* moe_status_string(int status);
 
-/* ABI version of this header; bumped on any incompatible change (3: FINALIZE workspace query takes k). */
+/* ABI version of this header; bumped on any incompatible change (3: FINALIZE workspace query takes k;
+ * 4: moe_router takes x_scale). */
 MOE_API int moe_abi_version(void);
 
 /* Reads and clears the device error word written by bounded waits that gave

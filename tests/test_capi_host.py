@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.moe_abi_version() == 3
+    assert L.moe_abi_version() == 4
     for s in range(8):
         assert L.moe_status_string(s)
     assert L.moe_status_string(99) == b"unknown status"
