@@ -49,24 +49,14 @@ struct PartialLogits {
   float* x_scale;               // ... turned into x's NVFP4 decode multiplier here
 };
 
+// Top-k and softmax of tokens [t0, t1), one warp per token (warps of the whole
+// block in turn); counts each selected expert in the shared histogram `hist`.
 template <int NV, bool PARTS>  // NV: logits per lane, NV * 32 >= E; PARTS: read partial sums
-__global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __restrict__ logits, RouteDims d,
-                                                              int32_t* __restrict__ topk_id,
-                                                              float* __restrict__ topk_w,
-                                                              int32_t* __restrict__ chunk_counts,
-                                                              PartialLogits pl) {
-  extern __shared__ int hist[];  // [E]
+MOE_DEVINL void route_tokens(const float* __restrict__ logits, const RouteDims& d, int t0, int t1,
+                             int32_t* __restrict__ topk_id, float* __restrict__ topk_w, int* hist,
+                             const PartialLogits& pl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (PARTS && pl.x_scale && blockIdx.x == 0 && threadIdx.x == 0) {
-    const float a = __uint_as_float(*pl.x_amax_bits);
-    *pl.x_scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);  // s = amax / (6 * 448), 1 when amax = 0
-  }
-  const int t0 = blockIdx.x * d.chunk_tokens;
-  const int t1 = min(d.T, t0 + d.chunk_tokens);
-  for (int e = threadIdx.x; e < d.E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
-
-  for (int t = t0 + warp; t < t1; t += kTopkThreads / 32) {
+  for (int t = t0 + warp; t < t1; t += blockDim.x / 32) {
     const float* row = logits + static_cast<int64_t>(t) * d.E;
     float v[NV];
     uint32_t taken = 0;
@@ -121,6 +111,29 @@ __global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __rest
       atomicAdd(&hist[my_i], 1);
     }
   }
+}
+
+// x's NVFP4 decode multiplier from the router GEMM's max |x| (block 0, thread 0).
+MOE_DEVINL void router_x_scale(const PartialLogits& pl) {
+  if (pl.x_scale && blockIdx.x == 0 && threadIdx.x == 0) {
+    const float a = __uint_as_float(*pl.x_amax_bits);
+    *pl.x_scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);  // s = amax / (6 * 448), 1 when amax = 0
+  }
+}
+
+template <int NV, bool PARTS>
+__global__ void __launch_bounds__(kTopkThreads) route_kernel(const float* __restrict__ logits, RouteDims d,
+                                                              int32_t* __restrict__ topk_id,
+                                                              float* __restrict__ topk_w,
+                                                              int32_t* __restrict__ chunk_counts,
+                                                              PartialLogits pl) {
+  extern __shared__ int hist[];  // [E]
+  if (PARTS) router_x_scale(pl);
+  const int t0 = blockIdx.x * d.chunk_tokens;
+  const int t1 = min(d.T, t0 + d.chunk_tokens);
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  route_tokens<NV, PARTS>(logits, d, t0, t1, topk_id, topk_w, hist, pl);
   __syncthreads();
   int32_t* out = chunk_counts + static_cast<int64_t>(blockIdx.x) * d.E;
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) out[e] = hist[e];
@@ -243,6 +256,65 @@ __global__ void __launch_bounds__(kRouteThreads) scatter_kernel(RouteDims d, con
   }
 }
 
+// The whole routing step in one block when every (token, slot) item fits one
+// chunk (T * k <= 256): top-k, expert offsets and the stable scatter, without
+// the scan and scatter launches (small decode batches are launch-bound).
+// 1024 threads, E <= 1024; dynamic shared memory 2 * E ints.
+template <int NV, bool PARTS>
+__global__ void __launch_bounds__(kTopkThreads) route_one_chunk_kernel(
+    const float* __restrict__ logits, RouteDims d, int32_t* __restrict__ topk_id, float* __restrict__ topk_w,
+    int32_t* __restrict__ expert_offsets, int32_t* __restrict__ pad_offsets, int32_t* __restrict__ perm_to_expanded,
+    int32_t* __restrict__ expanded_to_perm, int32_t* __restrict__ expanded_to_row, PartialLogits pl) {
+  extern __shared__ int sm[];
+  int* hist = sm;        // [E] items per expert, then each expert's first position
+  int* cnt = sm + d.E;   // [E] items of each expert placed so far
+  __shared__ int warp_tot[32];
+  if (PARTS) router_x_scale(pl);
+  for (int e = threadIdx.x; e < d.E; e += blockDim.x) { hist[e] = 0; cnt[e] = 0; }
+  __syncthreads();
+  route_tokens<NV, PARTS>(logits, d, 0, d.T, topk_id, topk_w, hist, pl);
+  __syncthreads();
+  // expert offsets and padded (128-row) offsets: thread e holds expert e
+  const int e = threadIdx.x;
+  const int total = e < d.E ? hist[e] : 0;
+  const int off = block_exclusive_scan(total, warp_tot);
+  const int padded = e < d.E ? ((total + 127) / 128) * 128 : 0;
+  const int poff = block_exclusive_scan(padded, warp_tot);
+  if (e < d.E) {
+    expert_offsets[e] = off;
+    pad_offsets[e] = poff;
+    if (e == d.E - 1) {
+      expert_offsets[d.E] = off + total;
+      pad_offsets[d.E] = poff + padded;
+    }
+    hist[e] = off;
+  }
+  __syncthreads();
+  // stable scatter: item i = t * k + j, ranked within its expert by i (warps in order, peers by lane)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = d.T * d.k;
+  const int i = threadIdx.x;
+  const bool valid = i < n;
+  const int ex = valid ? topk_id[i] : -1;
+  const unsigned active = __ballot_sync(0xffffffffu, valid);
+  unsigned peers = 0;
+  if (valid) peers = __match_any_sync(active, ex);
+  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+  for (int w = 0; w < kRouteThreads / 32; ++w) {
+    __syncthreads();
+    if (warp == w && valid) {
+      const int base = cnt[ex];
+      __syncwarp(active);
+      const int leader = __ffs(peers) - 1;
+      if (lane == leader) cnt[ex] = base + __popc(peers);
+      const int pos = hist[ex] + base + rank_in_warp;
+      perm_to_expanded[pos] = i;
+      expanded_to_perm[i] = pos;
+      expanded_to_row[i] = pad_offsets[ex] + (pos - expert_offsets[ex]);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -278,6 +350,24 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
   const size_t hist_bytes = sizeof(int) * E;
   const int nv = (E + 31) / 32;
   const PartialLogits pl{part, splits, NE, logits_out, x_amax_bits, x_scale};
+  if (d.n_chunks == 1) {
+    const size_t one_bytes = 2 * sizeof(int) * E;
+#define MOE_ROUTE1(NV)                                                                                           \
+  (part ? route_one_chunk_kernel<NV, true><<<1, kTopkThreads, one_bytes, st>>>(                                  \
+              logits, d, topk_id, topk_w, expert_offsets, pads, perm_to_expanded, expanded_to_perm, expanded_to_row, \
+              pl)                                                                                                \
+        : route_one_chunk_kernel<NV, false><<<1, kTopkThreads, one_bytes, st>>>(                                 \
+              logits, d, topk_id, topk_w, expert_offsets, pads, perm_to_expanded, expanded_to_perm, expanded_to_row, \
+              pl))
+    if (nv <= 1) MOE_ROUTE1(1);
+    else if (nv <= 2) MOE_ROUTE1(2);
+    else if (nv <= 4) MOE_ROUTE1(4);
+    else if (nv <= 8) MOE_ROUTE1(8);
+    else if (nv <= 16) MOE_ROUTE1(16);
+    else MOE_ROUTE1(32);
+#undef MOE_ROUTE1
+    return check_launch();
+  }
 #define MOE_ROUTE(NV)                                                                                         \
   (part ? route_kernel<NV, true><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl) \
         : route_kernel<NV, false><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl))
