@@ -469,25 +469,31 @@ def test_moe_forward_gated_matches_oracle(T, E, k, H, I):
     _check_layer(fwd, out, ref, h_scale, T, E, k, H, I)
 
 
-def test_timeout_path_reports_and_recovers():
-    """A pipeline stage that is never filled: the bounded waits give up, the kernel reports
-    MOE_ERR_TIMEOUT and returns; the context stays usable."""
-    counts, N, K = [32, 32], 128, 512
-    offs = counts_to_offsets(counts)
-    x = inputs.activations(64, K, seed=1)
-    w = inputs.expert_weights(2, N, K, 3)
-    codes, sf, s, dst = _routed_operand(x, offs)
-    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=False)
+def _run_with_timeout_hook(launch):
+    """Runs `launch` with the first pipeline stage never filled and a 50 ms wait bound; returns the error."""
     torch.cuda.synchronize()
     moe.device_error()
     moe.set_wait_timeout_ns(50_000_000)
     moe.debug_set_flags(1)
     try:
-        moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV))
-        code, where = moe.device_error()
+        launch()
+        return moe.device_error()
     finally:
         moe.debug_set_flags(0)
         moe.set_wait_timeout_ns(0)
+
+
+@pytest.mark.parametrize("counts", [[32, 32], [200, 150]])   # the 64-row (decode) and 128-row tile
+def test_timeout_path_reports_and_recovers(counts):
+    """A pipeline stage that is never filled: the bounded waits give up, the kernel reports
+    MOE_ERR_TIMEOUT and returns; the context stays usable."""
+    N, K = 128, 512
+    offs = counts_to_offsets(counts)
+    x = inputs.activations(int(offs[-1]), K, seed=1)
+    w = inputs.expert_weights(2, N, K, 3)
+    codes, sf, s, dst = _routed_operand(x, offs)
+    pw = moe.prepare_expert_weights(w.to(DEV), gate_up=False)
+    code, _ = _run_with_timeout_hook(lambda: moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV)))
     assert code == 6  # MOE_ERR_TIMEOUT
     out = moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw, torch.from_numpy(offs).to(DEV))
     torch.cuda.synchronize()
@@ -495,6 +501,41 @@ def test_timeout_path_reports_and_recovers():
     xc, xs, xsc = oracle.quantize_dynamic(x.float().numpy())
     ref = oracle.grouped_gemm(xc, xs, xsc, *oracle.quantize_weights(w.numpy()), offs, N, K)
     tol_check(bf16_to_np(out)[dst], ref, "after timeout")
+
+
+@pytest.mark.parametrize("epi", ["silu", "finalize"])
+def test_timeout_path_128_row_epilogues(epi):
+    """The same at the 128-row tile with the SiLU epilogue and with FINALIZE (two epilogue warp groups)."""
+    T, E, k, H, I = 512, 4, 2, 256, 128
+    x, logits, w13f, w2f = _layer_case(T, E, k, H, I)
+    fwd = moe.MoeForward(T, E, k, H, I)
+    pw13 = moe.prepare_expert_weights(w13f.to(DEV), gate_up=True)
+    pw2 = moe.prepare_expert_weights(w2f.to(DEV), gate_up=False)
+    ids, w = oracle.route(logits.numpy(), k)
+    offs, p2e, e2p = oracle.permute(ids, E)
+    pad = oracle.padded_offsets(offs.astype(np.int64))
+    assert (int(pad[-1]) - 127 * E) // E > 48  # the kernel picks its 128-row tile above 48 rows per expert
+    if epi == "silu":
+        codes, sf, s, dst = _routed_operand(torch.repeat_interleave(x, k, 0)[p2e], offs.astype(np.int64))
+
+        def launch():
+            moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw13, torch.from_numpy(offs).to(DEV), moe.EPI_SILU_MUL_QUANT,
+                                       h_scale=0.01)
+    else:
+        h = (torch.randn(T * k, I, generator=torch.Generator().manual_seed(2)) * 0.3)
+        codes, sf, s, dst = _routed_operand(h, offs.astype(np.int64))
+
+        def launch():
+            moe.moe_grouped_gemm_nvfp4(codes, sf, s, pw2, torch.from_numpy(offs).to(DEV), moe.EPI_FINALIZE,
+                                       perm_to_expanded=torch.from_numpy(p2e).to(DEV),
+                                       topk_w=torch.from_numpy(w).to(DEV), T=T, k=k)
+    code, _ = _run_with_timeout_hook(launch)
+    assert code == 6  # MOE_ERR_TIMEOUT
+    # the context still works: the layer runs and matches the oracle
+    out = fwd(x.to(DEV), logits.to(DEV), pw13, pw2, 0.01)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    assert torch.isfinite(out.float()).all()
 
 
 def test_forward_graph_replays_the_layer():
