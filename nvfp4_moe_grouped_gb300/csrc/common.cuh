@@ -77,18 +77,24 @@ MOE_DEVINL float route_exp(float x) {
   return __fmul_rn(p, two_n);
 }
 
-// e2m1 code of v: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even
-// code, saturating above 6; a magnitude-0 result is +0.
-// The code is the number of rounding boundaries below |v| (strict at the
-// boundaries that round down to an even code, inclusive at those that round up
-// to one).
-MOE_DEVINL uint32_t e2m1_encode(float v) {
-  const float a = fabsf(v);
-  const uint32_t c = static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-                     static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-                     static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
-                     static_cast<uint32_t>(a > 5.0f);
-  return (c != 0u && v < 0.0f) ? (c | 8u) : c;
+// e2m1 codes of eight values, v[i] in bits 4i..4i+3: the nearest of
+// {0, .5, 1, 1.5, 2, 3, 4, 6} with the sign, ties to the even code, saturating
+// above 6 (the hardware conversion, two values per instruction, the first
+// operand to the high nibble); then the sign bit is cleared wherever the
+// magnitude code is 0, so a value that rounds to zero is +0.
+MOE_DEVINL uint32_t e2m1x8(const float (&v)[8]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+      "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+      : "=r"(w)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  // bit 3 of every nibble whose magnitude (bits 0-2) is non-zero: m + 7 carries into it
+  const uint32_t nonzero = ((w & 0x77777777u) + 0x77777777u) & 0x88888888u;
+  return w & (0x77777777u | nonzero);
 }
 
 // e4m3 (fn) scale byte of a non-negative value: round to nearest even,
@@ -114,8 +120,13 @@ MOE_DEVINL uint32_t nvfp4_block_scale(float amax, float s, float* recip) {
   return sf;
 }
 
-MOE_DEVINL uint32_t nvfp4_code(float x, float recip) {
-  return (recip == 0.0f) ? 0u : e2m1_encode(__fmul_rn(x, recip));
+// Codes of x[0..7] under the block's reciprocal multiplier (0 when the block's
+// decoded scale is 0: every product is then a zero and every code 0).
+MOE_DEVINL uint32_t nvfp4_codes8(const float* x, float recip) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(x[i], recip);
+  return e2m1x8(v);
 }
 
 MOE_DEVINL float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }

@@ -619,11 +619,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
             }
             float recip;
             const uint32_t sfb = nvfp4_block_scale(amax, p.h_scale, &recip);
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) lo |= nvfp4_code(h[t], recip) << (4 * t);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) hi |= nvfp4_code(h[8 + t], recip) << (4 * t);
+            const uint32_t lo = nvfp4_codes8(h, recip), hi = nvfp4_codes8(h + 8, recip);
             const int64_t row = d.x_row + j0 + jj;
             const int i0 = d.mt * 64 + 16 * blk;
             *reinterpret_cast<uint2*>(p.h_codes + row * (I / 2) + i0 / 2) = make_uint2(lo, hi);

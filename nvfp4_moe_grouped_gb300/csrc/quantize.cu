@@ -41,27 +41,56 @@ MOE_DEVINL void load_block16(const void* x, int64_t row, int K, int blk, float (
   }
 }
 
-// Per-group absolute maximum: atomicMax on the bit pattern, which orders
-// non-negative floats like their values.
+// max |element| of one 16-byte vector of bf16 (8) or FP32 (4) values
 template <int IN_F32>
-__global__ void __launch_bounds__(256) amax_kernel(const void* __restrict__ x, int64_t rows_per_group, int K,
-                                                   uint32_t* __restrict__ amax_bits) {
-  const int g = blockIdx.y;
-  const int64_t nblk = rows_per_group * (K / 16);
-  const int64_t base_row = static_cast<int64_t>(g) * rows_per_group;
+MOE_DEVINL float abs_max_vec(const uint4 u) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
   float m = 0.0f;
-  for (int64_t b = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; b < nblk;
-       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int64_t r = base_row + b / (K / 16);
-    int c = static_cast<int>(b % (K / 16));
-    float v[16];
-    load_block16<IN_F32>(x, r, K, c, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+  for (int j = 0; j < 4; ++j) {
+    if (IN_F32) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[j])));
+    } else {
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    }
   }
+  return m;
+}
+
+// Per-group absolute maximum over the group's rows (contiguous, a multiple of 16
+// bytes long): 16-byte loads in a grid-stride loop, a block-wide reduction, then
+// one atomicMax per block on the bit pattern, which orders non-negative floats
+// like their values.
+constexpr int kAmaxThreads = 256;
+template <int IN_F32>
+__global__ void __launch_bounds__(kAmaxThreads) amax_kernel(const void* __restrict__ x, int64_t rows_per_group,
+                                                            int K, uint32_t* __restrict__ amax_bits) {
+  __shared__ float warp_max[kAmaxThreads / 32];
+  const int g = blockIdx.y;
+  constexpr int kPerVec = IN_F32 ? 4 : 8;  // elements per 16-byte vector
+  const int64_t n_vec = rows_per_group * K / kPerVec;
+  const uint4* v = reinterpret_cast<const uint4*>(x) + static_cast<int64_t>(g) * n_vec;
+  float m = 0.0f;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kAmaxThreads;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x;
+  for (; i + 3 * stride < n_vec; i += 4 * stride) {  // four loads in flight per thread
+    uint4 u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) u[j] = __ldg(v + i + j * stride);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, abs_max_vec<IN_F32>(u[j]));
+  }
+  for (; i < n_vec; i += stride) m = fmaxf(m, abs_max_vec<IN_F32>(__ldg(v + i)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(amax_bits + g, __float_as_uint(m));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 1; w < kAmaxThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
+    if (m > 0.0f) atomicMax(amax_bits + g, __float_as_uint(m));
+  }
 }
 
 // Decode multiplier of every group from its amax (used when the quantise kernel
@@ -105,13 +134,8 @@ MOE_DEVINL uint32_t quantize_block16(const void* x, int64_t row, int K, int blk,
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
   float recip;
   const uint32_t sfb = nvfp4_block_scale(amax, s, &recip);
-  uint32_t l = 0, h = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) l |= nvfp4_code(v[i], recip) << (4 * i);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) h |= nvfp4_code(v[8 + i], recip) << (4 * i);
-  *lo = l;
-  *hi = h;
+  *lo = nvfp4_codes8(v, recip);
+  *hi = nvfp4_codes8(v + 8, recip);
   return sfb;
 }
 
@@ -143,15 +167,26 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
     s = __ldg(scale + g);
   }
   if (K % 64 == 0) {
+    // The row's destinations, one per lane (fan <= 32), loaded up front alongside x
+    // and broadcast in the loop below instead of one dependent load per store.
+    int64_t my_dst = 0;
+    if (lane < fan) {
+      const int64_t item = src * fan + lane;
+      my_dst = dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item;
+    }
     // this warp's slice: quads [32 * slice, 32 * slice + 32), one per lane
-    for (int q = 32 * slice + lane; q < min(K / 64, 32 * slice + 32); q += 32) {
-      uint32_t c[8];
-      uint32_t sf4 = 0;
+    const int q = 32 * slice + lane;
+    const bool act = q < K / 64;
+    uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t sf4 = 0;
+    if (act) {
 #pragma unroll
       for (int b = 0; b < 4; ++b) sf4 |= quantize_block16<IN_F32>(x, src, K, 4 * q + b, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
+    }
+    {
       for (int j = 0; j < fan; ++j) {
-        const int64_t item = src * fan + j;
-        const int64_t dst = dst_row ? static_cast<int64_t>(__ldg(dst_row + item)) : item;
+        const int64_t dst = __shfl_sync(0xffffffffu, my_dst, j);
+        if (!act) continue;
         uint8_t *c0, *c1, *sf_at;
         if (LAYOUT == 2) {
           const int kt_count = (K + 255) / 256;
@@ -234,15 +269,17 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
   if (dynamic_scale) {
     uint32_t* amax = static_cast<uint32_t*>(ws);
     if (cudaMemsetAsync(amax, 0, sizeof(uint32_t) * groups, st) != cudaSuccess) return MOE_ERR_CUDA;
-    int64_t nblk = rows_per_group * (K / 16);
-    int bx = static_cast<int>((nblk + 255) / 256);
-    int cap = (num_sms() * 8 + groups - 1) / groups;
-    if (bx > cap) bx = cap < 1 ? 1 : cap;
+    // four 16-byte vectors per thread per pass; about four blocks per SM over all groups
+    const int64_t n_vec = rows_per_group * K / (in_dtype == MOE_IN_F32 ? 4 : 8);
+    int64_t bx64 = (n_vec + 4 * kAmaxThreads - 1) / (4 * kAmaxThreads);
+    const int cap = (num_sms() * 4 + groups - 1) / groups;
+    if (bx64 > cap) bx64 = cap < 1 ? 1 : cap;
+    const int bx = static_cast<int>(bx64);
     dim3 grid(bx, groups);
     if (in_dtype == MOE_IN_F32)
-      amax_kernel<1><<<grid, 256, 0, st>>>(x, rows_per_group, K, amax);
+      amax_kernel<1><<<grid, kAmaxThreads, 0, st>>>(x, rows_per_group, K, amax);
     else
-      amax_kernel<0><<<grid, 256, 0, st>>>(x, rows_per_group, K, amax);
+      amax_kernel<0><<<grid, kAmaxThreads, 0, st>>>(x, rows_per_group, K, amax);
   }
   const bool covers_all_rows = (src_div > 1) || (n_items == src_rows);
   if (dynamic_scale && (n_items == 0 || !covers_all_rows))

@@ -82,6 +82,47 @@ def test_quantize_static_scale_and_zero_rows():
     assert np.array_equal(sf.cpu().numpy(), sf_ref)
 
 
+def test_quantize_rounding_boundaries_bitexact():
+    """Every e2m1 rounding boundary (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5), one FP32 step either side of it,
+    the grid values, signed zeros, tiny and subnormal values and products above 6 (saturation), in blocks
+    whose decoded scale is exactly 1 (block max 6 at s = 1) or rounds below the block max (6.2, 7.5)."""
+    f32 = np.float32
+    bounds = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    probes = []
+    for b in bounds:
+        b = f32(b)
+        probes += [b, np.nextafter(b, f32(0)), np.nextafter(b, f32(np.inf))]
+    probes += [0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, 0.0, 1e-30, 1e-40, 1e-45, 0.2499, 5.999]
+    probes = np.array(probes, dtype=f32)
+    probes = np.concatenate([probes, -probes, np.array([-0.0], dtype=f32)])
+    blocks = []
+    for anchor in (6.0, 6.2, 7.5):
+        vals = probes * f32(anchor / 6.0) if anchor != 6.0 else probes
+        vals = np.concatenate([vals, np.array([anchor * 0.99, -anchor * 0.999], dtype=f32)])
+        for i in range(0, len(vals), 15):
+            blk = np.zeros(16, dtype=f32)
+            chunk = vals[i:i + 15]
+            pos = i // 15 % 16                       # the anchor at varying positions
+            rest = [j for j in range(16) if j != pos]
+            blk[pos] = anchor if (i // 15) % 2 == 0 else -anchor
+            blk[rest[:len(chunk)]] = chunk
+            blocks.append(blk)
+    while len(blocks) % 16:
+        blocks.append(np.zeros(16, dtype=f32))
+    x = np.stack(blocks).reshape(-1, 256)
+    codes_ref, sf_ref = oracle.quantize(x, 1.0)
+    codes, sf, _ = moe.nvfp4_quantize(torch.from_numpy(x).to(DEV), torch.tensor([1.0], dtype=torch.float32,
+                                                                                device=DEV))
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+    # and through bf16 input (the activations' type): the values that bf16 holds exactly
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    codes_ref, sf_ref = oracle.quantize(xb.float().numpy(), 1.0)
+    codes, sf, _ = moe.nvfp4_quantize(xb.to(DEV), torch.tensor([1.0], dtype=torch.float32, device=DEV))
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+    assert np.array_equal(codes.cpu().numpy(), codes_ref)
+
+
 @pytest.mark.parametrize("gate_up,K", [(True, 320), (False, 512), (False, 128)])
 def test_quantize_weights_grouped_blocked_bitexact(gate_up, K):
     E, N = 3, 256
