@@ -183,7 +183,33 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
 #pragma unroll
       for (int b = 0; b < 4; ++b) sf4 |= quantize_block16<IN_F32>(x, src, K, 4 * q + b, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
     }
-    {
+    if (LAYOUT != 2) {
+      // Linear codes: the slice's codes form one contiguous span of 32 B per quad.  Lane l
+      // holds 16-byte chunks 2l and 2l+1; after this transpose it holds chunks l and 32 + l,
+      // so each destination takes two fully coalesced 512-byte stores.
+      const int nq = min(32, K / 64 - 32 * slice);  // quads in this slice
+      const int src_a = lane >> 1, src_b = 16 + (lane >> 1);
+      const bool odd = (lane & 1) != 0;
+      uint32_t ca[4], cb[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t a_lo = __shfl_sync(0xffffffffu, c[t], src_a), a_hi = __shfl_sync(0xffffffffu, c[4 + t], src_a);
+        const uint32_t b_lo = __shfl_sync(0xffffffffu, c[t], src_b), b_hi = __shfl_sync(0xffffffffu, c[4 + t], src_b);
+        ca[t] = odd ? a_hi : a_lo;
+        cb[t] = odd ? b_hi : b_lo;
+      }
+      const bool st_a = lane < 2 * nq, st_b = 32 + lane < 2 * nq;
+      for (int j = 0; j < fan; ++j) {
+        const int64_t dst = __shfl_sync(0xffffffffu, my_dst, j);
+        uint8_t* span = codes + dst * (K / 2) + 32 * (32 * slice);
+        if (st_a) *reinterpret_cast<uint4*>(span + 16 * lane) = make_uint4(ca[0], ca[1], ca[2], ca[3]);
+        if (st_b) *reinterpret_cast<uint4*>(span + 512 + 16 * lane) = make_uint4(cb[0], cb[1], cb[2], cb[3]);
+        if (act) {
+          uint8_t* sf_at = (LAYOUT == 1) ? sf + tiled_sf_offset(dst, 4 * q, K) : sf + dst * (K / 16) + 4 * q;
+          *reinterpret_cast<uint32_t*>(sf_at) = sf4;
+        }
+      }
+    } else {
       for (int j = 0; j < fan; ++j) {
         const int64_t dst = __shfl_sync(0xffffffffu, my_dst, j);
         if (!act) continue;
