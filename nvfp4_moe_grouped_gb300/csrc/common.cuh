@@ -24,6 +24,23 @@ int32_t* device_error_word();          // device address of {code, where}
 uint64_t wait_timeout_ns();            // bound of every device-side wait
 int num_sms();                          // SM count of the current device
 moe_status check_launch();              // maps cudaGetLastError to a status
+// Pieces of the public calls that the layer's graph schedules on their own:
+// the activation quantiser's amax pass (into `amax_ws`, nvfp4_quantize's
+// workspace), the quantiser itself with amax_mode 0 = static scale, 1 = compute
+// the amax here, 2 = the amax is already in the workspace, and the grouped GEMM
+// with or without clearing its FINALIZE accumulator (the bytes to clear, 0 when
+// FINALIZE gathers rows instead, come from finalize_accumulator_bytes).
+moe_status quantize_amax_enqueue(const void* x, int in_dtype, int64_t rows_per_group, int K, int groups,
+                                 uint32_t* amax_ws, cudaStream_t st);
+moe_status quantize_enqueue(const void* x, int in_dtype, int64_t src_rows, int K, int groups, float* tensor_scale,
+                            int amax_mode, int64_t n_items, int src_div, const int32_t* dst_row, uint8_t* codes,
+                            uint8_t* sf, int sf_layout, int64_t dst_rows_alloc, void* ws, size_t ws_bytes,
+                            cudaStream_t st);
+moe_status grouped_gemm_enqueue(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                const uint8_t* b_blocked, const float* b_scale, const int32_t* expert_offsets, int E,
+                                int64_t a_rows_alloc, int N, int K, int epilogue, const moe_epilogue_args* ep,
+                                void* out, void* ws, size_t ws_bytes, bool clear_accumulator, cudaStream_t st);
+size_t finalize_accumulator_bytes(int T, int N);
 // cuTensorMapEncodeTiled from the driver, or nullptr when the driver lacks it.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

@@ -83,9 +83,14 @@ moe_status forward_check(const uint16_t* x, const float* logits, const moe_weigh
 // `w_gate` the first stage is moe_router (logits GEMM, routing, and x's decode
 // multiplier from the GEMM's own pass over x) and the quantiser takes that
 // multiplier as a static scale; otherwise the logits are an input.
+// With `side` (a second stream, used while capturing the layer's graph) two
+// steps leave the chain: the activation quantiser's amax pass runs beside the
+// routing (it reads only x), and the FINALIZE accumulator is cleared beside the
+// gate_up GEMM; jev[0..3] are the events of those forks and joins.
 moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t* w_gate, const moe_weights* w,
                           int T, int E, int k, int H, int I, float h_scale, uint16_t* out, void* ws,
-                          const moe_forward_layout& L, cudaStream_t stream, cudaEvent_t* ev, bool external) {
+                          const moe_forward_layout& L, cudaStream_t stream, cudaEvent_t* ev, bool external,
+                          cudaStream_t side = nullptr, cudaEvent_t* jev = nullptr) {
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
   auto mark = [&](int i) -> moe_status {
@@ -107,8 +112,19 @@ moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t
   float* hs = static_cast<float*>(at(L.h_scale));
   uint8_t* h_codes = static_cast<uint8_t*>(at(L.h_codes));
   uint8_t* h_sf = static_cast<uint8_t*>(at(L.h_sf));
+  auto fork = [&](cudaEvent_t e, cudaStream_t from, cudaStream_t to) -> moe_status {
+    return cudaEventRecord(e, from) == cudaSuccess && cudaStreamWaitEvent(to, e, 0) == cudaSuccess ? MOE_OK
+                                                                                                  : MOE_ERR_CUDA;
+  };
+  const bool par = side != nullptr && jev != nullptr;
+  const bool amax_beside = par && !w_gate;  // with w_gate the router's GEMM supplies x's multiplier
   moe_status s = mark(0);
   if (s != MOE_OK) return s;
+  if (amax_beside) {
+    if ((s = fork(jev[0], stream, side)) != MOE_OK) return s;
+    s = quantize_amax_enqueue(x, MOE_IN_BF16, T, H, 1, static_cast<uint32_t*>(at(L.quant_ws)), side);
+    if (s != MOE_OK || cudaEventRecord(jev[1], side) != cudaSuccess) return s != MOE_OK ? s : MOE_ERR_CUDA;
+  }
   if (w_gate) {
     s = moe_router(x, w_gate, T, E, H, k, nullptr, x_scale, topk_id, topk_w, offs, p2e, e2p, e2r, at(L.total),
                    moe_router_workspace_size(T, E, H, k), stream);
@@ -117,25 +133,35 @@ moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t
                           moe_route_permute_workspace_size(T, E, k), stream);
   }
   if (s != MOE_OK || (s = mark(1)) != MOE_OK) return s;
-  s = nvfp4_quantize(x, MOE_IN_BF16, T, H, 1, x_scale, w_gate ? 0 : 1, R, k, e2r, x_codes, x_sf, MOE_SF_TILED,
-                     L.padded_rows, at(L.quant_ws), nvfp4_quantize_workspace_size(1), stream);
+  if (amax_beside && cudaStreamWaitEvent(stream, jev[1], 0) != cudaSuccess) return MOE_ERR_CUDA;
+  s = quantize_enqueue(x, MOE_IN_BF16, T, H, 1, x_scale, w_gate ? 0 : (amax_beside ? 2 : 1), R, k, e2r, x_codes,
+                       x_sf, MOE_SF_TILED, L.padded_rows, at(L.quant_ws), nvfp4_quantize_workspace_size(1), stream);
   if (s != MOE_OK || (s = mark(2)) != MOE_OK) return s;
+  const size_t acc_bytes = finalize_accumulator_bytes(T, H);
+  const bool clear_beside = par && acc_bytes > 0;
+  if (clear_beside) {
+    if ((s = fork(jev[2], stream, side)) != MOE_OK) return s;
+    if (cudaMemsetAsync(at(L.gemm_ws), 0, acc_bytes, side) != cudaSuccess ||
+        cudaEventRecord(jev[3], side) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   moe_epilogue_args ep{};
   ep.h_scale = h_scale;
   ep.h_scale_out = hs;
   ep.h_codes = h_codes;
   ep.h_sf = h_sf;
-  s = moe_grouped_gemm_nvfp4(x_codes, x_sf, x_scale, w->w13, w->w13_scale, offs, E, L.padded_rows, 2 * I, H,
-                             MOE_EPI_SILU_MUL_QUANT, &ep, nullptr, nullptr, 0, stream);
+  s = grouped_gemm_enqueue(x_codes, x_sf, x_scale, w->w13, w->w13_scale, offs, E, L.padded_rows, 2 * I, H,
+                           MOE_EPI_SILU_MUL_QUANT, &ep, nullptr, nullptr, 0, true, stream);
   if (s != MOE_OK || (s = mark(3)) != MOE_OK) return s;
+  if (clear_beside && cudaStreamWaitEvent(stream, jev[3], 0) != cudaSuccess) return MOE_ERR_CUDA;
   moe_epilogue_args ep2{};
   ep2.perm_to_expanded = p2e;
   ep2.topk_w = topk_w;
   ep2.T = T;
   ep2.k = k;
-  s = moe_grouped_gemm_nvfp4(h_codes, h_sf, hs, w->w2, w->w2_scale, offs, E, L.padded_rows, H, I, MOE_EPI_FINALIZE,
-                             &ep2, out, at(L.gemm_ws), moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H),
-                             stream);
+  s = grouped_gemm_enqueue(h_codes, h_sf, hs, w->w2, w->w2_scale, offs, E, L.padded_rows, H, I, MOE_EPI_FINALIZE,
+                           &ep2, out, at(L.gemm_ws), moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H),
+                           !clear_beside, stream);
   if (s != MOE_OK) return s;
   return mark(4);
 }
@@ -198,15 +224,30 @@ extern "C" moe_status moe_forward_graph_create(const uint16_t* x, const float* l
   if (!device_error_word() || num_sms() < 1) return MOE_ERR_CUDA;
   moe_forward_graph* g = new moe_forward_graph();
   g->timed = stage_events != 0;
-  cudaStream_t st = nullptr;
+  cudaStream_t st = nullptr, side = nullptr;
+  cudaEvent_t jev[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaGraph_t raw = nullptr;
+  auto release_capture_objects = [&]() {
+    for (auto& e : jev)
+      if (e) { cudaEventDestroy(e); e = nullptr; }
+    if (side) { cudaStreamDestroy(side); side = nullptr; }
+    if (st) { cudaStreamDestroy(st); st = nullptr; }
+  };
   auto fail = [&](moe_status code) {
     if (raw) cudaGraphDestroy(raw);
-    if (st) cudaStreamDestroy(st);
+    release_capture_objects();
     graph_release(g);
     return code;
   };
   if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  // The untimed graph takes the amax pass and the accumulator clear off the
+  // chain (forward_stages); the timed one keeps every step between its stage
+  // events.
+  if (!g->timed) {
+    if (cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) != cudaSuccess) return fail(MOE_ERR_CUDA);
+    for (auto& e : jev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  }
   if (g->timed)
     for (auto& e : g->ev)
       if (cudaEventCreate(&e) != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -216,15 +257,15 @@ extern "C" moe_status moe_forward_graph_create(const uint16_t* x, const float* l
   if (s != MOE_OK) return fail(s);
   if (cudaStreamSynchronize(st) != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return fail(MOE_ERR_CUDA);
-  s = forward_stages(x, logits, nullptr, w, T, E, k, H, I, h_scale, out, ws, L, st, g->timed ? g->ev : nullptr, true);
+  s = forward_stages(x, logits, nullptr, w, T, E, k, H, I, h_scale, out, ws, L, st, g->timed ? g->ev : nullptr, true,
+                     side, g->timed ? nullptr : jev);
   cudaError_t ce = cudaStreamEndCapture(st, &raw);
   if (s != MOE_OK) return fail(s);
   if (ce != cudaSuccess || !raw) return fail(MOE_ERR_CUDA);
   if (cudaGraphInstantiate(&g->exec, raw, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
   cudaGraphDestroy(raw);
   raw = nullptr;
-  cudaStreamDestroy(st);
-  st = nullptr;
+  release_capture_objects();
   *graph = g;
   return MOE_OK;
 }

@@ -718,11 +718,17 @@ extern "C" size_t moe_grouped_gemm_workspace_size(int epilogue, int T, int k, in
   return ((b + 255) / 256) * 256;
 }
 
-extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
-                                             const uint8_t* b_blocked, const float* b_scale,
-                                             const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,
-                                             int epilogue, const moe_epilogue_args* ep, void* out, void* ws,
-                                             size_t ws_bytes, void* stream) {
+namespace moe {
+
+size_t finalize_accumulator_bytes(int T, int N) {
+  if (T < 1 || N < 1 || finalize_gathers(T, N)) return 0;
+  return static_cast<size_t>(T) * N * sizeof(float);
+}
+
+moe_status grouped_gemm_enqueue(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                const uint8_t* b_blocked, const float* b_scale, const int32_t* expert_offsets, int E,
+                                int64_t a_rows_alloc, int N, int K, int epilogue, const moe_epilogue_args* ep,
+                                void* out, void* ws, size_t ws_bytes, bool clear_accumulator, cudaStream_t st) {
   if (!a_codes || !a_sf || !a_scale || !b_blocked || !b_scale || !expert_offsets) return MOE_ERR_INVALID_ARG;
   if (E < 1 || a_rows_alloc < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_SILU_MUL_QUANT && epilogue != MOE_EPI_FINALIZE)
@@ -787,8 +793,7 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
     const moe_status ps = bn == 64 ? prepare_gemm<64, 1>() : two_groups ? prepare_gemm<128, 2>() : prepare_gemm<128, 1>();
     if (ps != MOE_OK) return ps;
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (epilogue == MOE_EPI_FINALIZE && !p.fin_gather) {
+  if (clear_accumulator && epilogue == MOE_EPI_FINALIZE && !p.fin_gather) {
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
@@ -803,4 +808,15 @@ extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8
                               static_cast<int64_t>(ep->T) * N, st);
   }
   return MOE_OK;
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                             const uint8_t* b_blocked, const float* b_scale,
+                                             const int32_t* expert_offsets, int E, int64_t a_rows_alloc, int N, int K,
+                                             int epilogue, const moe_epilogue_args* ep, void* out, void* ws,
+                                             size_t ws_bytes, void* stream) {
+  return grouped_gemm_enqueue(a_codes, a_sf, a_scale, b_blocked, b_scale, expert_offsets, E, a_rows_alloc, N, K,
+                              epilogue, ep, out, ws, ws_bytes, true, static_cast<cudaStream_t>(stream));
 }

@@ -263,10 +263,30 @@ extern "C" size_t nvfp4_quantize_workspace_size(int groups) {
   return static_cast<size_t>((groups * 4 + 255) / 256) * 256;
 }
 
-extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows, int K, int groups,
-                                     float* tensor_scale, int dynamic_scale, int64_t n_items, int src_div,
-                                     const int32_t* dst_row, uint8_t* codes, uint8_t* sf, int sf_layout,
-                                     int64_t dst_rows_alloc, void* ws, size_t ws_bytes, void* stream) {
+namespace moe {
+
+moe_status quantize_amax_enqueue(const void* x, int in_dtype, int64_t rows_per_group, int K, int groups,
+                                 uint32_t* amax, cudaStream_t st) {
+  if (cudaMemsetAsync(amax, 0, sizeof(uint32_t) * groups, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // four 16-byte vectors per thread per pass; about four blocks per SM over all groups
+  const int64_t n_vec = rows_per_group * K / (in_dtype == MOE_IN_F32 ? 4 : 8);
+  int64_t bx64 = (n_vec + 4 * kAmaxThreads - 1) / (4 * kAmaxThreads);
+  const int cap = (num_sms() * 4 + groups - 1) / groups;
+  if (bx64 > cap) bx64 = cap < 1 ? 1 : cap;
+  const int bx = static_cast<int>(bx64);
+  dim3 grid(bx, groups);
+  if (in_dtype == MOE_IN_F32)
+    amax_kernel<1><<<grid, kAmaxThreads, 0, st>>>(x, rows_per_group, K, amax);
+  else
+    amax_kernel<0><<<grid, kAmaxThreads, 0, st>>>(x, rows_per_group, K, amax);
+  return check_launch();
+}
+
+moe_status quantize_enqueue(const void* x, int in_dtype, int64_t src_rows, int K, int groups, float* tensor_scale,
+                            int amax_mode, int64_t n_items, int src_div, const int32_t* dst_row, uint8_t* codes,
+                            uint8_t* sf, int sf_layout, int64_t dst_rows_alloc, void* ws, size_t ws_bytes,
+                            cudaStream_t st) {
+  const int dynamic_scale = amax_mode != 0;
   if (!x || !tensor_scale || !codes || (!sf && sf_layout != MOE_SF_BLOCKED)) return MOE_ERR_INVALID_ARG;
   if (src_rows < 1 || K < 16 || groups < 1 || n_items < 0 || src_div < 1 || dst_rows_alloc < 1)
     return MOE_ERR_INVALID_ARG;
@@ -290,22 +310,10 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
   const int n_slices = (K % 64 == 0) ? (K / 64 + 31) / 32 : 1;
   const int64_t blocks = (n_src * n_slices + kQuantWarps - 1) / kQuantWarps;
   if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t rows_per_group = src_rows / groups;
-  if (dynamic_scale) {
-    uint32_t* amax = static_cast<uint32_t*>(ws);
-    if (cudaMemsetAsync(amax, 0, sizeof(uint32_t) * groups, st) != cudaSuccess) return MOE_ERR_CUDA;
-    // four 16-byte vectors per thread per pass; about four blocks per SM over all groups
-    const int64_t n_vec = rows_per_group * K / (in_dtype == MOE_IN_F32 ? 4 : 8);
-    int64_t bx64 = (n_vec + 4 * kAmaxThreads - 1) / (4 * kAmaxThreads);
-    const int cap = (num_sms() * 4 + groups - 1) / groups;
-    if (bx64 > cap) bx64 = cap < 1 ? 1 : cap;
-    const int bx = static_cast<int>(bx64);
-    dim3 grid(bx, groups);
-    if (in_dtype == MOE_IN_F32)
-      amax_kernel<1><<<grid, kAmaxThreads, 0, st>>>(x, rows_per_group, K, amax);
-    else
-      amax_kernel<0><<<grid, kAmaxThreads, 0, st>>>(x, rows_per_group, K, amax);
+  if (amax_mode == 1) {
+    const moe_status s = quantize_amax_enqueue(x, in_dtype, rows_per_group, K, groups, static_cast<uint32_t*>(ws), st);
+    if (s != MOE_OK) return s;
   }
   const bool covers_all_rows = (src_div > 1) || (n_items == src_rows);
   if (dynamic_scale && (n_items == 0 || !covers_all_rows))
@@ -332,4 +340,15 @@ extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_ro
 #undef MOE_QLAUNCH
   }
   return check_launch();
+}
+
+}  // namespace moe
+
+extern "C" moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows, int K, int groups,
+                                     float* tensor_scale, int dynamic_scale, int64_t n_items, int src_div,
+                                     const int32_t* dst_row, uint8_t* codes, uint8_t* sf, int sf_layout,
+                                     int64_t dst_rows_alloc, void* ws, size_t ws_bytes, void* stream) {
+  return quantize_enqueue(x, in_dtype, src_rows, K, groups, tensor_scale, dynamic_scale ? 1 : 0, n_items, src_div,
+                          dst_row, codes, sf, sf_layout, dst_rows_alloc, ws, ws_bytes,
+                          static_cast<cudaStream_t>(stream));
 }
