@@ -121,7 +121,8 @@ struct Cfg {
   static constexpr int bars = tok_w + 2 * BN * 4;            // uint64 [3*kStages + 2*kAccBufs + 1]
   static constexpr int misc = bars + (3 * kStages + 2 * kAccBufs + 1) * 8;  // tmem base, abort flag
   static constexpr int last = misc + 16;                     // int [kProducers][kStages]
-  static constexpr int sched = last + kProducers * kStages * 4;  // int [3][kMaxExperts+1]
+  static constexpr int info = last + kProducers * kStages * 4;  // int [kStages]: MMA N and scale column offset
+  static constexpr int sched = info + kStages * 4;           // int [3][kMaxExperts+1]
   static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
   static constexpr int smem_bytes = total + 1024;            // + alignment slack
   static_assert(smem_bytes <= 232448, "shared memory budget");
@@ -162,7 +163,7 @@ struct Unit {
 // The expert owning unit u (start[e] <= u < start[e + 1]), searched from `e`, an
 // expert at or before the owner: every role walks its units in increasing order,
 // so the search gallops forward from the previous owner instead of bisecting all
-// E experts (shared-memory loads are slow on the MMA-issuing thread).
+// E experts.
 MOE_DEVINL int find_expert_from(const int* start, int E, int u, int e) {
   int lo = e, step = 1, hi = e + 1;
   while (hi < E && start[hi] <= u) {
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
   uint64_t* mma_done = acc_empty + C::kAccBufs;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::misc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::misc + 4);
+  int* s_info = reinterpret_cast<int*>(smem + C::info);
   int* unit_start = reinterpret_cast<int*>(smem + C::sched);
   int* pad_start = unit_start + (kMaxExperts + 1);
   int* off = pad_start + (kMaxExperts + 1);
@@ -328,7 +330,11 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
-        if (!d.valid) continue;
+        if (!d.valid) {  // offsets that place a unit outside the routed-row allocation: stop the launch
+          if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+          *s_abort = 1;
+          break;
+        }
         const uint8_t* w_src = p.w_blocked + static_cast<int64_t>(d.e * MT + d.mt) * KT * kWStageBytes;
         const uint8_t* sfx_src = p.x_sf + static_cast<int64_t>(d.x_row / 128) * (K / 64) * 512;
         for (int kt = 0; kt < KT; ++kt, ++fill) {
@@ -384,7 +390,6 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int acc_i = 0;
-      int e_hint = 0;
       bool ok = true;
       // Every instruction on this thread delays the next MMA issue, and at a
       // 128-row tile the tensor core finishes an MMA about as fast as one is
@@ -393,9 +398,10 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
       // stages in order, so the later stage being ready implies the earlier).
       const uint64_t adesc0 = smem_desc(smem_u32(s_w), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(s_x), 16, 1024, 2);
+      // The unit's MMA N and scale column offset come from the staging warps with
+      // the unit's first stage (s_info): decoding the unit here would put a chain
+      // of dependent shared-memory loads on this thread once per unit.
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++acc_i) {
-        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
-        if (!d.valid) { --acc_i; continue; }
         const int b = acc_i % C::kAccBufs;
         if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
           if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 2);
@@ -404,10 +410,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * C::kAccCols;
-        const uint32_t idesc = idesc_mxf4nvf4(d.n_mma);
-        // The routed rows' scale atoms cover a 128-row block; this unit's rows start
-        // (x_row % 128) / 32 TMEM columns into each atom's four columns.
-        const uint32_t sfx_col_off = static_cast<uint32_t>((d.x_row & 127) >> 5);
+        uint32_t idesc = 0, sfx_col_off = 0;
         for (int kt = 0; kt < KT; ++kt) {
           if ((kt & 1) == 0) {
             // sf_ready implies full: the staging warps saw the stage's copies land.
@@ -421,6 +424,11 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
               break;
             }
             tc_fence_after();
+            if (kt == 0) {
+              const int info = s_info[stage];
+              idesc = idesc_mxf4nvf4(info & 0xFFFF);
+              sfx_col_off = static_cast<uint32_t>(info >> 16);
+            }
           }
           const uint32_t sf_col = tmem_base + C::kSfTmemBase + stage * kSfSlotCols;
           // start-address field of the descriptors: byte address / 16
@@ -463,7 +471,13 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
-      if (!d.valid) continue;
+      if (!d.valid) {
+        if (lane == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+          *s_abort = 1;
+        }
+        break;
+      }
       for (int kt = 0; kt < KT; ++kt) {
         const bool got = mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort);
         if (!__all_sync(0xffffffffu, got)) {
@@ -487,6 +501,9 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
         tmem_st_32cols(tmem_base + quad_lane + C::kSfTmemBase + stage * kSfSlotCols, v);
         tmem_st_wait();
         tc_fence_before();
+        // the unit's MMA N and the routed rows' scale column offset within each atom
+        // ((x_row % 128) / 32) for the MMA thread, published with the unit's first stage
+        if (kt == 0 && warp == 6 && lane == 0) s_info[stage] = d.n_mma | (((d.x_row & 127) >> 5) << 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_ready[stage]);
         if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -507,9 +524,11 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
       const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
       if (!d.valid) {
-        if (et == 0) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
-        --acc_i;
-        continue;
+        if (et == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+          *s_abort = 1;
+        }
+        break;
       }
       if (acc_i % C::kEpiGroups != eg) continue;  // the other group drains this unit
       const int b = acc_i % C::kAccBufs;
