@@ -288,6 +288,10 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  * expert on average) or 128 (otherwise) routed rows as MMA N.
  * Requires K % 64 == 0, N % 128 == 0,
  * E <= 1024, a_rows_alloc % 128 == 0, all pointers 16-byte aligned.
+ * Device-side errors (read with moe_device_error): expert offsets that place a
+ * tile outside the a_rows_alloc rows stop the launch with MOE_ERR_INVALID_ARG
+ * (the output is then undefined); a wait past the bound set by
+ * moe_set_wait_timeout_ns reports MOE_ERR_TIMEOUT.
  * ------------------------------------------------------------------------- */
 typedef struct {
   /* MOE_EPI_SILU_MUL_QUANT */
