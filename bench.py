@@ -829,6 +829,20 @@ def run_gated(args, rank, world, local_rank):
     layer_bytes = ab["layer"] - T * E * 4 + E * H * 2   # the gate matrix is read instead of the logits
     hbm_peak, _, peak_kind = peaks()
     gbs = layer_bytes / (ms / 1e3) / 1e9
+    if T * k / max(1, ab["active_experts"]) > 48:
+        # compute-bound regime (as for the layer workload): the whole graph's expert-GEMM FLOPs against the
+        # measured dense FP4 MMA rate
+        fp4_peak = moe.fp4_mma_peak_tflops()
+        flops = 2.0 * T * k * (2 * I * H + H * I)
+        tf = flops / (ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": "whole layer with the router (one CUDA graph)", "achieved": tf,
+                "peak": fp4_peak, "unit": "TFLOP/s", "frac": tf / fp4_peak,
+                "peak_kind": "measured (this GPU's dense NVFP4 MMA rate, moe_fp4_mma_probe)", "traffic": None,
+                "algorithmic_flops_per_launch": flops, "launch_ms": ms, "hbm_gbs": gbs}
+    else:
+        roof = {"bound": "hbm", "kernel": "whole layer with the router (one CUDA graph)", "achieved": gbs,
+                "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
+                "traffic": None, "algorithmic_bytes_per_launch": layer_bytes, "launch_ms": ms}
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": whole_job_rate(T, world, ms), "unit": "tokens/s", "n_gpus": world,
@@ -838,9 +852,7 @@ def run_gated(args, rank, world, local_rank):
             "config": {"workload": f"moe_layer_gated_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf
                                                                                   else "_uniform"),
                        "l2": "weights exceed L2; no flush" if flush is None else "256 MB written between steps"},
-            "roofline": {"bound": "hbm", "kernel": "whole layer with the router (one CUDA graph)", "achieved": gbs,
-                         "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind,
-                         "traffic": None, "algorithmic_bytes_per_launch": layer_bytes, "launch_ms": ms},
+            "roofline": roof,
             "same_layer_fed_logits_ms": ms_plain,
             # router GEMM, routing (3), quantiser, gate_up, down, FP32->BF16 per step
             "gpu_launches": 8 * args.steps, "clocks": clk.summary()}), flush=True)
