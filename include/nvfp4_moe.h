@@ -288,10 +288,12 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  * expert on average) or 128 (otherwise) routed rows as MMA N.
  * Requires K % 64 == 0, N % 128 == 0,
  * E <= 1024, a_rows_alloc % 128 == 0, all pointers 16-byte aligned.
- * Device-side errors (read with moe_device_error): expert offsets that place a
- * tile outside the a_rows_alloc rows stop the launch with MOE_ERR_INVALID_ARG
- * (the output is then undefined); a wait past the bound set by
- * moe_set_wait_timeout_ns reports MOE_ERR_TIMEOUT.
+ * Device-side errors (read with moe_device_error): expert offsets that would
+ * place a tile before row 0, past the a_rows_alloc rows or (FINALIZE) outside
+ * the T*k routed items stop the launch with MOE_ERR_INVALID_ARG; other
+ * inconsistent offsets give an undefined output without any access outside
+ * the operands.  A wait past the bound set by moe_set_wait_timeout_ns reports
+ * MOE_ERR_TIMEOUT.
  * ------------------------------------------------------------------------- */
 typedef struct {
   /* MOE_EPI_SILU_MUL_QUANT */
@@ -402,10 +404,13 @@ MOE_API moe_status moe_forward_gated(const uint16_t* x, const uint16_t* w_gate, 
  * relaunch; the workspace, weights and out must stay valid and must not be
  * used by anything else while a launch of the graph may run.  With
  * stage_events != 0 the graph records timing events between the four stages
- * (route+permute, quantise x, gate_up GEMM, down GEMM + FINALIZE);
- * moe_forward_graph_stage_ms waits for the last launch and writes the five
- * durations in ms (the four stages, then the whole layer) to ms[5] (host).
- * Creation makes CUDA objects (a stream, events, the executable graph) but no
+ * (route+permute, quantise x, gate_up GEMM, down GEMM + FINALIZE), every step
+ * in series; moe_forward_graph_stage_ms waits for the last launch and writes
+ * the five durations in ms (the four stages, then the whole layer) to ms[5]
+ * (host).  With stage_events == 0 two steps run on side branches of the graph:
+ * the activation amax pass beside the routing, and the clearing of the
+ * FINALIZE accumulator beside the gate_up GEMM.  The results are the same.
+ * Creation makes CUDA objects (streams, events, the executable graph) but no
  * device buffers; destroy releases them.  *graph (host) receives the handle.
  * ------------------------------------------------------------------------- */
 typedef struct moe_forward_graph moe_forward_graph;

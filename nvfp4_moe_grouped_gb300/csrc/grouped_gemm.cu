@@ -18,7 +18,7 @@
 //     weight tile is streamed from HBM once per BN routed rows and the tensor
 //     core never computes padding rows of M.
 //   * The routed-row tile BN is picked per launch from the rows-per-expert
-//     regime: BN = 64 with 7 pipeline stages for decode, BN = 128 with 4
+//     regime: BN = 64 with 7 pipeline stages for decode, BN = 128 with 5
 //     stages when experts see more rows (prefill).
 //   * Work unit = (expert, BN-row block of its routed rows, 128-row weight
 //     tile), full K.  Units are ordered expert-major so the CTAs running
@@ -33,17 +33,19 @@
 //     streams a contiguous 18 KB run of HBM.
 //   * Warp roles: warp 0 issues the copies (weights: bulk copy, evict-first;
 //     routed rows: 2D tensor-map loads with 128-byte swizzle and a bulk copy
-//     of their scale atoms, evict-last).  In the decode tile warps 10-12 issue
-//     copies too, each one stage fill in four: one issuing thread gets its bulk
-//     copies served one after another.  Warps 6-9 move each stage's scale atoms
-//     from shared into tensor memory (tcgen05.st, one warp per lane quadrant),
-//     warp 1 owns tensor memory and issues only the tcgen05.mma instructions
-//     and their commits, warps 2-5 drain the accumulator (tcgen05.ld) and run
-//     the epilogue; in the prefill tile warps 10-13 form a second epilogue
-//     group that drains every other unit, since one group could not keep up
-//     with the FINALIZE and SiLU epilogues there.  A tcgen05.cp of the
-//     scales on the MMA thread would serialise with the MMA that reads them:
-//     at decode that halved the weight-streaming rate.  Several TMEM
+//     of their scale atoms, evict-last).  With one epilogue group warps 10-12
+//     issue copies too, each one stage fill in four: one issuing thread gets
+//     its bulk copies served one after another.  Warps 6-9 move each stage's
+//     scale atoms from shared into tensor memory (tcgen05.st, one warp per lane
+//     quadrant) and hand the MMA thread each unit's MMA N and scale column
+//     offset with the unit's first stage.  Warp 1 owns tensor memory and
+//     issues only the tcgen05.mma instructions and their commits; warps 2-5
+//     drain the accumulator (tcgen05.ld) and run the epilogue.  A FINALIZE
+//     launch at the 128-row tile has warps 10-13 as a second epilogue group
+//     that drains every other unit, since one group could not keep up with
+//     its atomics there.  A tcgen05.cp of the scales on the MMA thread would
+//     serialise with the MMA that reads them: at decode that halved the
+//     weight-streaming rate.  Several TMEM
 //     accumulators (four for the 64-row tile, two for the 128-row one) let the
 //     epilogue of one unit overlap the mainloops of the next ones; every
 //     stage has its own TMEM scale slot, recycled by the same commit that
@@ -150,6 +152,7 @@ struct GemmParams {
   int fin_gather;             // FINALIZE: 1 = store weighted rows per expanded item (summed later), 0 = atomics
   int mt_chunk;               // weight tiles per column chunk of the unit order (N/128 = one chunk)
   int64_t rows_alloc;         // rows of the routed-row operand (bounds every access to it)
+  int64_t items;              // FINALIZE: T * k, the length of perm_to_expanded; otherwise unbounded
   int32_t* err;
   uint64_t timeout_ns;
   int debug_flags;            // bit 0: the producer skips the first stage (bounded-wait test hook)
@@ -157,7 +160,7 @@ struct GemmParams {
 
 struct Unit {
   int e, nb, mt, rows, n_mma, x_row, m_off;
-  bool valid;  // false when the offsets place the unit outside the routed-row allocation
+  bool valid;  // false when the offsets place the unit outside the operands (the launch then stops)
 };
 
 // The expert owning unit u (start[e] <= u < start[e + 1]), searched from `e`, an
@@ -184,7 +187,7 @@ MOE_DEVINL int find_expert_from(const int* start, int E, int u, int e) {
 // consecutive units (the chunk's weight tiles).
 template <int BN>
 MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MTC, int U,
-                            int64_t rows_alloc, int& e_hint) {
+                            int64_t rows_alloc, int64_t items, int& e_hint) {
   Unit d;
   const int c = u / U;
   const int uc = u - c * U;
@@ -199,7 +202,11 @@ MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, 
   if (d.n_mma > BN) d.n_mma = BN;
   d.x_row = pad_start[d.e] + d.nb * BN;
   d.m_off = off[d.e] + d.nb * BN;
-  d.valid = d.rows > 0 && static_cast<int64_t>(d.x_row) + BN <= rows_alloc;
+  // offsets as the routing writes them always pass; corrupted ones (decreasing,
+  // negative, past the allocation or the item count) stop the launch instead of
+  // reaching memory outside the operands
+  d.valid = d.rows > 0 && d.x_row >= 0 && static_cast<int64_t>(d.x_row) + BN <= rows_alloc && d.m_off >= 0 &&
+            static_cast<int64_t>(d.m_off) + d.rows <= items;
   return d;
 }
 
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
       int e_hint = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
+        const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, p.items, e_hint);
         if (!d.valid) {  // offsets that place a unit outside the routed-row allocation: stop the launch
           if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
           *s_abort = 1;
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     int e_hint = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, p.items, e_hint);
       if (!d.valid) {
         if (lane == 0) {
           if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
@@ -522,7 +529,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     int acc_i = 0;
     int e_hint = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++acc_i) {
-      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, e_hint);
+      const Unit d = decode_unit<BN>(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, p.items, e_hint);
       if (!d.valid) {
         if (et == 0) {
           if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
@@ -793,6 +800,7 @@ moe_status grouped_gemm_enqueue(const uint8_t* a_codes, const uint8_t* a_sf, con
   }
   if (p.mt_chunk == 0) p.mt_chunk = N / kBM;
   p.rows_alloc = a_rows_alloc;
+  p.items = epilogue == MOE_EPI_FINALIZE ? static_cast<int64_t>(ep->T) * ep->k : INT64_MAX;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
   p.debug_flags = gemm_debug_flags();

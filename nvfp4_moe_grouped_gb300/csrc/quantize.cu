@@ -8,8 +8,13 @@
 // q = e2m1(x / (e4m3(sf) s)) -- the reading stated in nvfp4_moe.h.
 //
 // HBM-bound: one read of x, one write of codes (K/2 bytes per row) and scales
-// (K/16 bytes per row).  One warp per output row; each lane owns 16-element
-// blocks lane, lane+32, ... so a warp streams contiguous 1 KB (bf16) chunks.
+// (K/16 bytes per row) per destination.  One warp per source row and slice of
+// 32 x 64 elements; each lane owns 64 consecutive elements (four 16-element
+// blocks), so a warp reads 4 KB of bf16 contiguously, quantises them once and
+// writes them to every routed row that reads the source row.  The e2m1 codes
+// come from the hardware conversion (e2m1x8 in common.cuh).  The dynamic
+// per-tensor scale needs the amax of all of x first: a separate pass
+// (amax_kernel).
 #include "common.cuh"
 
 namespace moe {
