@@ -71,6 +71,26 @@ def test_quantize_linear_bf16_bitexact(rows, K):
     assert s.cpu().numpy()[0] == np.float32(s_ref)
 
 
+@pytest.mark.parametrize("dtype,groups,rows,K", [(torch.float32, 1, 96, 512), (torch.bfloat16, 4, 200, 320),
+                                                  (torch.float32, 3, 129, 1024), (torch.bfloat16, 5, 5, 64)])
+def test_quantize_dynamic_per_group_linear_bitexact(dtype, groups, rows, K):
+    """Dynamic decode multipliers per group of rows (each group's own amax) in the linear layout, from FP32
+    and bf16 input: every group's codes, scales and multiplier as the oracle quantises that group alone.
+    One group is all zeros (multiplier 1, zero codes and scales)."""
+    x = inputs.activations(rows * groups, K, seed=rows + groups).float() * 3.0
+    if groups > 1:
+        x[rows:2 * rows] = 0.0
+    x = x.to(dtype)
+    codes, sf, s = moe.nvfp4_quantize(x.to(DEV), None, groups=groups)
+    codes, sf, s = codes.cpu().numpy(), sf.cpu().numpy(), s.cpu().numpy()
+    for g in range(groups):
+        xr = x[g * rows:(g + 1) * rows].float().numpy()
+        c_ref, sf_ref, s_ref = oracle.quantize_dynamic(xr)
+        assert s[g] == np.float32(s_ref), g
+        assert np.array_equal(codes[g * rows:(g + 1) * rows], c_ref), g
+        assert np.array_equal(sf[g * rows:(g + 1) * rows], sf_ref), g
+
+
 def test_quantize_static_scale_and_zero_rows():
     x = inputs.activations(64, 512, seed=3).float()
     x[5] = 0.0
@@ -173,7 +193,10 @@ def test_finalize_matches_oracle(T, k, N):
 
 # ------------------------------------------------------------------ router (logits GEMM + routing)
 
-@pytest.mark.parametrize("T,E,k,H", [(16, 8, 2, 256), (129, 40, 4, 512), (300, 256, 8, 1024), (1024, 256, 8, 6144)])
+# T*k <= 256: one routing kernel; up to 1024 tokens: fewer chunks than SMs (half-width blocks that load all
+# partial sums at once); 6144 tokens: 192 chunks, full-width blocks
+@pytest.mark.parametrize("T,E,k,H", [(16, 8, 2, 256), (129, 40, 4, 512), (300, 256, 8, 1024), (1024, 256, 8, 6144),
+                                     (6144, 256, 8, 512)])
 def test_router_matches_oracle(T, E, k, H):
     """Logits within the FP32 summation-order bound of the oracle's FP64 sums; the routing is exactly the
     oracle's routing of the GPU's logits, and agrees with the oracle's own logits except at near-ties."""
