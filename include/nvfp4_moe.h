@@ -98,7 +98,7 @@ enum { MOE_EPI_NONE = 0, MOE_EPI_SILU_MUL_QUANT = 1, MOE_EPI_FINALIZE = 2 };
 MOE_API const char* moe_status_string(int status);
 
 /* ABI version of this header; bumped on any incompatible change (3: FINALIZE workspace query takes k;
- * 4: moe_router takes x_scale). */
+ * 4: moe_router takes x_scale; 5: moe_finalize takes y_rows). */
 MOE_API int moe_abi_version(void);
 
 /* Reads and clears the device error word written by bounded waits that gave
@@ -161,10 +161,14 @@ MOE_API moe_status moe_route_permute(const float* logits, int T, int E, int k, i
  * moe_route_permute_static_scratch_bytes() bytes (1 MiB) in the library's
  * device memory, reserved on every GPU that loads the library until the
  * process exits; a call whose moe_route_permute_workspace_size(T, E, k)
- * exceeds it returns MOE_ERR_WORKSPACE without launching anything.  The call
- * allocates nothing.  The first call on a device looks up the array's device
- * address (once per device, with that device current); make that first call
- * before any stream capture.  Every call shares the one array, so calls that
+ * exceeds it returns MOE_ERR_WORKSPACE without launching anything (shapes
+ * outside the limits below get MOE_ERR_UNSUPPORTED first, as from
+ * moe_route_permute; the size is checked before the pointers).  The call
+ * allocates nothing.  Every call looks up the array's device address in the
+ * current device's context (cudaGetSymbolAddress, which allocates nothing),
+ * so the address never outlives a context; the first call on a device may
+ * load the library's device code, so make it before any stream capture.
+ * Every call shares the one array, so calls that
  * can overlap on the GPU (different streams, or different host threads) race
  * and must be serialised by the caller.  Nothing in the array needs clearing
  * between calls: the kernels write every scratch word before they read it.
@@ -324,15 +328,17 @@ MOE_API moe_status moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t*
  *   Calculation" (FP32 accumulator, BF16 output).
  *   out[t][n] = bf16_rn( sum_{j<k} topk_w[t][j] * y[row_of_item[t*k+j]][n] ),
  *   summed in FP32 in slot order (deterministic).
- *   y            bf16 [*][N]
+ *   y            bf16 [y_rows][N]
  *   topk_w       f32 [T][k]
  *   row_of_item  i32 [T*k]: the row of y holding item t*k+j (expanded_to_perm
  *                for an unpadded y, expanded_to_row for a padded one)
  *   out          bf16 [T][N]
- * Requires N % 8 == 0.
+ * Requires N % 8 == 0, y_rows >= 1.  A row_of_item entry outside [0, y_rows)
+ * is not read: its term is left out and MOE_ERR_INVALID_ARG is recorded in the
+ * device error word (moe_device_error, location 8).
  * ------------------------------------------------------------------------- */
-MOE_API moe_status moe_finalize(const uint16_t* y, const float* topk_w, const int32_t* row_of_item, int T, int k, int N,
-                        uint16_t* out, void* stream);
+MOE_API moe_status moe_finalize(const uint16_t* y, int64_t y_rows, const float* topk_w, const int32_t* row_of_item,
+                                int T, int k, int N, uint16_t* out, void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_fp4_mma_probe -- measurement aid: enqueues one launch that issues
@@ -340,9 +346,20 @@ MOE_API moe_status moe_finalize(const uint16_t* y, const float* topk_w, const in
  * M = 128, N = 256, K = 64, operands in shared memory, no global-memory
  * traffic) on each of `blocks` CTAs (0 = one per SM).  The caller times the
  * launch on `stream`; *flops_per_launch (host) receives the FLOPs it performs.
+ * iters is at most 1,000,000 and at most one per 200 ns of the wait bound
+ * (moe_set_wait_timeout_ns), so the launch's final wait cannot run out while
+ * MMAs are still in flight; larger values return MOE_ERR_INVALID_ARG.
  * Gives the dense FP4 tensor rate the prefill roofline is measured against.
  * ------------------------------------------------------------------------- */
 MOE_API moe_status moe_fp4_mma_probe(int iters, int blocks, double* flops_per_launch, void* stream);
+
+/* moe_fp4_mma_probe_pair -- the same measurement for the CTA-pair MMA form
+ * (tcgen05 cta_group::2): `pairs` clusters of two CTAs (0 = as many as can be
+ * resident at once), one thread of each pair issuing `iters` M = 256, N = 256,
+ * K = 64 MMAs whose operand halves sit in the two CTAs' shared memory.  Same
+ * limits on iters as moe_fp4_mma_probe; *flops_per_launch (host) receives the
+ * FLOPs one launch performs. */
+MOE_API moe_status moe_fp4_mma_probe_pair(int iters, int pairs, double* flops_per_launch, void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_forward -- the fused MoE layer: route + permute, quantise x into the

@@ -77,16 +77,19 @@ def debug_set_flags(flags: int) -> None:
     _L().moe_debug_set_flags(int(flags))
 
 
-def fp4_mma_peak_tflops(iters: int = 20000, reps: int = 5) -> float:
-    """Dense NVFP4 MMA rate of this GPU (TFLOP/s), timed with CUDA events over `reps` probe launches."""
+def fp4_mma_peak_tflops(iters: int = 20000, reps: int = 5, pair: bool = False) -> float:
+    """Dense NVFP4 MMA rate of this GPU (TFLOP/s), timed with CUDA events over `reps` probe launches:
+    M = 128 MMAs on every SM (pair=False) or the CTA-pair form, M = 256 over two SMs (pair=True)."""
     L = _L()
+    probe = L.moe_fp4_mma_probe_pair if pair else L.moe_fp4_mma_probe
+    name = "moe_fp4_mma_probe_pair" if pair else "moe_fp4_mma_probe"
     flops = ctypes.c_double(0.0)
     s = torch.cuda.current_stream()
-    _check("moe_fp4_mma_probe", L.moe_fp4_mma_probe(1000, 0, ctypes.byref(flops), _stream(s)))  # warm-up
+    _check(name, probe(1000, 0, ctypes.byref(flops), _stream(s)))  # warm-up
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s)
     for _ in range(reps):
-        _check("moe_fp4_mma_probe", L.moe_fp4_mma_probe(iters, 0, ctypes.byref(flops), _stream(s)))
+        _check(name, probe(iters, 0, ctypes.byref(flops), _stream(s)))
     b.record(s)
     b.synchronize()
     return flops.value * reps / (a.elapsed_time(b) / 1e3) / 1e12
@@ -290,8 +293,8 @@ def moe_finalize(y: torch.Tensor, topk_w: torch.Tensor, row_of_item: torch.Tenso
     N = y.shape[1]
     if out is None:
         out = _empty((T, N), torch.bfloat16, y.device)
-    _check("moe_finalize", _L().moe_finalize(_ptr(y), _ptr(topk_w), _ptr(row_of_item), T, k, N, _ptr(out),
-                                             _stream(stream)))
+    _check("moe_finalize", _L().moe_finalize(_ptr(y), y.shape[0], _ptr(topk_w), _ptr(row_of_item), T, k, N,
+                                             _ptr(out), _stream(stream)))
     return out
 
 

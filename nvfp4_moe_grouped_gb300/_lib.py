@@ -68,8 +68,9 @@ SIGNATURES = {
     "moe_grouped_gemm_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
     "moe_grouped_gemm_nvfp4": (c_int, [c_void_p] * 6 + [c_int, c_int64, c_int, c_int, c_int, c_void_p, c_void_p,
                                                         c_void_p, c_size_t, c_void_p]),
-    "moe_finalize": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "moe_finalize": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "moe_fp4_mma_probe": (c_int, [c_int, c_int, c_void_p, c_void_p]),
+    "moe_fp4_mma_probe_pair": (c_int, [c_int, c_int, c_void_p, c_void_p]),
     "moe_forward_workspace_size": (c_size_t, [c_int] * 5),
     "moe_forward_gated_workspace_size": (c_size_t, [c_int] * 5),
     "moe_forward_gated": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,

@@ -1,7 +1,5 @@
 // capi.cu -- the C ABI's housekeeping: status names, the device error word of
 // the bounded waits, the wait bound, the debug hook, device properties.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace moe {
@@ -14,19 +12,13 @@ uint64_t g_timeout_ns = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 }  // namespace
 
+// Device address of g_device_error in the current device's context, looked up
+// on every call (cheap, allocates nothing): a cached address could outlive its
+// context after cudaDeviceReset or under another context on the same device.
 int32_t* device_error_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  static std::mutex mu;
-  static int32_t* ptrs[64] = {nullptr};
-  if (dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int32_t*>(p);
-  }
-  return ptrs[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+  return static_cast<int32_t*>(p);
 }
 
 uint64_t wait_timeout_ns() { return g_timeout_ns; }
@@ -72,7 +64,7 @@ extern "C" const char* moe_status_string(int status) {
   }
 }
 
-extern "C" int moe_abi_version(void) { return 4; }
+extern "C" int moe_abi_version(void) { return 5; }
 
 extern "C" moe_status moe_device_error(int32_t* code, int32_t* where) {
   if (!code || !where) return MOE_ERR_INVALID_ARG;

@@ -325,9 +325,103 @@ MOE_DEVINL uint64_t smem_desc(uint32_t start, uint32_t lbo, uint32_t sbo, uint32
 }
 
 // Instruction descriptor of kind::mxf4nvf4: e2m1 A and B (format 1), both
-// K-major, ue4m3 scales (bit 23 = 0), dense, M = 128.
-__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int n) {
-  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+// K-major, ue4m3 scales (bit 23 = 0), dense, M = 128 (or m).
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int n, int m = 128) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ----------------------------------------------------------------------------
+// CTA pairs (tcgen05 cta_group::2).  Two CTAs of a cluster (ranks 2c and
+// 2c + 1) form a pair; one thread of the even CTA issues MMAs with M = 256:
+// A rows 0-127 from the even CTA's shared memory and rows 128-255 from the odd
+// CTA's (same offset), B rows [0, N/2) from the even CTA's and [N/2, N) from
+// the odd CTA's, the accumulator rows of each CTA in its own tensor memory.
+// Every tcgen05 instruction of a kernel that uses pairs names cta_group::2:
+// allocation and release are made by one warp of EACH CTA together.
+// ----------------------------------------------------------------------------
+MOE_DEVINL uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+MOE_DEVINL uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+MOE_DEVINL uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs arrives; returns once all have (release/acquire at cluster scope).
+MOE_DEVINL void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Shared-memory address `addr` (of this CTA) mapped into CTA `rank` of the cluster.
+MOE_DEVINL uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier given by its cluster address (this CTA's or the peer's).
+MOE_DEVINL void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+MOE_DEVINL bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait_bounded for a barrier that threads of the peer CTA arrive on.
+MOE_DEVINL bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, volatile int* abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+MOE_DEVINL void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+MOE_DEVINL void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MOE_DEVINL void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// The pair form of mma_mxf4nvf4 (M = 256 over the two CTAs), issued by one thread of the even CTA.
+MOE_DEVINL void mma_mxf4nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// Arrives once on the mbarrier at the same shared-memory offset in each CTA of
+// `cta_mask` when every tcgen05 operation issued so far by this thread has
+// completed (the pair's MMAs write both CTAs' tensor memory).
+MOE_DEVINL void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
 }
 
 // Instruction descriptor of kind::f16 with bf16 A and B (format 1), FP32 D

@@ -18,7 +18,8 @@ namespace {
 __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ y,
                                                        const float* __restrict__ topk_w,
                                                        const int32_t* __restrict__ row_of_item, int T, int k,
-                                                       int N, uint16_t* __restrict__ out) {
+                                                       int N, int64_t y_rows, uint16_t* __restrict__ out,
+                                                       int32_t* err) {
   const int vec_per_row = N / 8;
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= static_cast<int64_t>(T) * vec_per_row) return;
@@ -31,6 +32,10 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
     const int64_t item = static_cast<int64_t>(t) * k + j;
     const float w = __ldg(topk_w + item);
     const int64_t r = __ldg(row_of_item + item);
+    if (r < 0 || r >= y_rows) {  // a row map outside y: report it and leave the term out
+      record_error(err, MOE_ERR_INVALID_ARG, 8);
+      continue;
+    }
     uint4 u = __ldg(reinterpret_cast<const uint4*>(y + r * N + c));
     uint32_t p[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -105,16 +110,18 @@ moe_status launch_f32_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStr
 
 using namespace moe;
 
-extern "C" moe_status moe_finalize(const uint16_t* y, const float* topk_w, const int32_t* row_of_item, int T, int k,
-                                   int N, uint16_t* out, void* stream) {
+extern "C" moe_status moe_finalize(const uint16_t* y, int64_t y_rows, const float* topk_w, const int32_t* row_of_item,
+                                   int T, int k, int N, uint16_t* out, void* stream) {
   if (!y || !topk_w || !row_of_item || !out) return MOE_ERR_INVALID_ARG;
-  if (T < 1 || k < 1 || N < 8) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || k < 1 || N < 8 || y_rows < 1) return MOE_ERR_INVALID_ARG;
   if (N % 8) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(y) || !aligned16(out)) return MOE_ERR_MISALIGNED;
   int64_t threads = static_cast<int64_t>(T) * (N / 8);
   int64_t blocks = (threads + 255) / 256;
   if (blocks > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  int32_t* err = device_error_word();
+  if (!err) return MOE_ERR_CUDA;
   finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      y, topk_w, row_of_item, T, k, N, out);
+      y, topk_w, row_of_item, T, k, N, y_rows, out, err);
   return check_launch();
 }

@@ -229,6 +229,108 @@ MOE_DEVINL bool epi_any(int g, bool pred) {
   return r != 0;
 }
 
+// ---- epilogue bodies of one 32-column accumulator chunk (shared by both kernels) ----
+// r: the chunk as loaded by tcgen05.ld (this thread's weight row, 32 routed rows);
+// jn: routed rows of the chunk that exist.
+
+// NONE: out[row0 + jj][col] = bf16(alpha * acc).
+MOE_DEVINL void epi_chunk_none(const uint32_t (&r)[32], int jn, int64_t row0, int64_t col, int N, float alpha,
+                               uint16_t* out) {
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj)
+    if (jj < jn) out[(row0 + jj) * N + col] = float_to_bf16_bits(alpha * __uint_as_float(r[jj]));
+}
+
+// FINALIZE: 4x4 transposes inside each lane quad (two shuffle rounds) give lane
+// 4g+i the four consecutive output columns 32q+4g .. +3 of routed rows i, i+4,
+// ..., i+28 of the chunk: one 16-byte vector atomic (or store) per 4 outputs, a
+// warp covering four 128-byte runs per instruction, with no shared-memory round
+// trip or barrier.  acc_col: the accumulator at column (tile column + 32q +
+// 4(lane/4)); tok/w: destination row and weight x alpha per routed row of the chunk.
+MOE_DEVINL void epi_chunk_finalize(uint32_t (&r)[32], int lane, int jn, const int* tok, const float* w, float* acc_col,
+                                   int N, bool gather) {
+  const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
+#pragma unroll
+  for (int sb = 0; sb < 8; ++sb) {
+    float a0 = __uint_as_float(r[4 * sb]), a1 = __uint_as_float(r[4 * sb + 1]);
+    float a2 = __uint_as_float(r[4 * sb + 2]), a3 = __uint_as_float(r[4 * sb + 3]);
+    // rows {0,1} x cols {2,3} <-> rows {2,3} x cols {0,1}
+    float t0 = __shfl_xor_sync(0xffffffffu, b1 ? a0 : a2, 2);
+    float t1 = __shfl_xor_sync(0xffffffffu, b1 ? a1 : a3, 2);
+    if (b1) { a0 = t0; a1 = t1; } else { a2 = t0; a3 = t1; }
+    // then within each 2x2 block
+    t0 = __shfl_xor_sync(0xffffffffu, b0 ? a0 : a1, 1);
+    t1 = __shfl_xor_sync(0xffffffffu, b0 ? a2 : a3, 1);
+    if (b0) { a0 = t0; a2 = t1; } else { a1 = t0; a3 = t1; }
+    r[4 * sb] = __float_as_uint(a0);
+    r[4 * sb + 1] = __float_as_uint(a1);
+    r[4 * sb + 2] = __float_as_uint(a2);
+    r[4 * sb + 3] = __float_as_uint(a3);
+  }
+#pragma unroll
+  for (int sb = 0; sb < 8; ++sb) {
+    const int jj = 4 * sb + (lane & 3);
+    if (jj < jn) {
+      const int t = tok[jj];
+      if (t >= 0) {
+        const float wt = w[jj];
+        const float4 v = make_float4(wt * __uint_as_float(r[4 * sb]), wt * __uint_as_float(r[4 * sb + 1]),
+                                     wt * __uint_as_float(r[4 * sb + 2]), wt * __uint_as_float(r[4 * sb + 3]));
+        float4* dst = reinterpret_cast<float4*>(acc_col + static_cast<int64_t>(t) * N);
+        if (gather)
+          *dst = v;
+        else
+          atomicAdd(dst, v);
+      }
+    }
+  }
+}
+
+// SILU_MUL_QUANT on a gate_up tile whose rows 0-63 are gate rows and rows
+// 64-127 the matching up rows: the chunk (128 tile rows x 32 routed rows) is
+// staged in shared memory, then each of the group's 128 threads (et) takes one
+// routed row and one 16-wide block of the 64 outputs, so an NVFP4 block (amax,
+// scale, codes) lives in one thread's registers.  row0: routed row of the
+// chunk's first column; i_tile: the tile's first output column (64 per tile).
+struct SiluOut {
+  float h_scale;
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+  float* h_f32;
+  int I;
+};
+MOE_DEVINL void epi_chunk_silu(const uint32_t (&r)[32], int m, int et, int eg, int jn, float alpha, float* s_epi_g,
+                               int64_t row0, int i_tile, const SiluOut& o) {
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) s_epi_g[jj * kEpiStride + m] = alpha * __uint_as_float(r[jj]);
+  epi_bar(eg);
+  const int jj = et >> 2, blk = et & 3;
+  if (jj < jn) {
+    const float* gp = s_epi_g + jj * kEpiStride + 16 * blk;
+    float h[16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const float g = gp[t];
+      h[t] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), gp[64 + t]);
+      amax = fmaxf(amax, fabsf(h[t]));
+    }
+    float recip;
+    const uint32_t sfb = nvfp4_block_scale(amax, o.h_scale, &recip);
+    const uint32_t lo = nvfp4_codes8(h, recip), hi = nvfp4_codes8(h + 8, recip);
+    const int64_t row = row0 + jj;
+    const int i0 = i_tile + 16 * blk;
+    *reinterpret_cast<uint2*>(o.h_codes + row * (o.I / 2) + i0 / 2) = make_uint2(lo, hi);
+    o.h_sf[tiled_sf_offset(row, i0 / 16, o.I)] = static_cast<uint8_t>(sfb);
+    if (o.h_f32) {
+      float4* dst = reinterpret_cast<float4*>(o.h_f32 + row * o.I + i0);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) dst[t] = make_float4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
+    }
+  }
+  epi_bar(eg);
+}
+
 template <int BN, int EG>
 __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xt,
@@ -568,95 +670,21 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
         }
         epi_bar(eg);
       }
+      const SiluOut so{p.h_scale, p.h_codes, p.h_sf, p.h_f32, N / 2};
       for (int j0 = 0; j0 < d.rows; j0 += 32) {
         uint32_t r[32];
         tmem_ld_32cols(taddr + j0, r);
         tmem_ld_wait();
         const int jn = min(32, d.rows - j0);
         if (p.epilogue == MOE_EPI_NONE) {
-          uint16_t* out = static_cast<uint16_t*>(p.out);
-          const int64_t col = static_cast<int64_t>(d.mt) * kBM + m;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
-            if (jj < jn)
-              out[static_cast<int64_t>(d.x_row + j0 + jj) * N + col] =
-                  float_to_bf16_bits(alpha * __uint_as_float(r[jj]));
+          epi_chunk_none(r, jn, d.x_row + j0, static_cast<int64_t>(d.mt) * kBM + m, N, alpha,
+                         static_cast<uint16_t*>(p.out));
         } else if (p.epilogue == MOE_EPI_FINALIZE) {
-          // 4x4 transposes inside each lane quad (two shuffle rounds) give lane
-          // 4g+i the four consecutive output columns 32q+4g .. +3 of routed rows
-          // i, i+4, ..., i+28 of the chunk: one 16-byte vector atomic (or store)
-          // per 4 outputs, a warp covering four 128-byte runs per instruction,
-          // with no shared-memory round trip or barrier.
-          const bool b1 = (lane & 2) != 0, b0 = (lane & 1) != 0;
-#pragma unroll
-          for (int sb = 0; sb < 8; ++sb) {
-            float a0 = __uint_as_float(r[4 * sb]), a1 = __uint_as_float(r[4 * sb + 1]);
-            float a2 = __uint_as_float(r[4 * sb + 2]), a3 = __uint_as_float(r[4 * sb + 3]);
-            // rows {0,1} x cols {2,3} <-> rows {2,3} x cols {0,1}
-            float t0 = __shfl_xor_sync(0xffffffffu, b1 ? a0 : a2, 2);
-            float t1 = __shfl_xor_sync(0xffffffffu, b1 ? a1 : a3, 2);
-            if (b1) { a0 = t0; a1 = t1; } else { a2 = t0; a3 = t1; }
-            // then within each 2x2 block
-            t0 = __shfl_xor_sync(0xffffffffu, b0 ? a0 : a1, 1);
-            t1 = __shfl_xor_sync(0xffffffffu, b0 ? a2 : a3, 1);
-            if (b0) { a0 = t0; a2 = t1; } else { a1 = t0; a3 = t1; }
-            r[4 * sb] = __float_as_uint(a0);
-            r[4 * sb + 1] = __float_as_uint(a1);
-            r[4 * sb + 2] = __float_as_uint(a2);
-            r[4 * sb + 3] = __float_as_uint(a3);
-          }
-          float* acc = static_cast<float*>(p.out) + static_cast<int64_t>(d.mt) * kBM + 32 * q + 4 * (lane >> 2);
-#pragma unroll
-          for (int sb = 0; sb < 8; ++sb) {
-            const int jj = 4 * sb + (lane & 3);
-            if (jj < jn) {
-              const int tok = tok_tab[j0 + jj];
-              if (tok >= 0) {
-                const float w = w_tab[j0 + jj];
-                const float4 v = make_float4(w * __uint_as_float(r[4 * sb]), w * __uint_as_float(r[4 * sb + 1]),
-                                             w * __uint_as_float(r[4 * sb + 2]), w * __uint_as_float(r[4 * sb + 3]));
-                float4* dst = reinterpret_cast<float4*>(acc + static_cast<int64_t>(tok) * N);
-                if (p.fin_gather)
-                  *dst = v;
-                else
-                  atomicAdd(dst, v);
-              }
-            }
-          }
+          epi_chunk_finalize(r, lane, jn, tok_tab + j0, w_tab + j0,
+                             static_cast<float*>(p.out) + static_cast<int64_t>(d.mt) * kBM + 32 * q + 4 * (lane >> 2),
+                             N, p.fin_gather != 0);
         } else {
-          // gate_up tile: rows 0-63 are gate rows, rows 64-127 the matching up rows.
-          // Stage the chunk (128 tile rows x 32 routed rows) in shared memory, then
-          // give each thread one routed row and one 16-wide block of the 64 outputs,
-          // so an NVFP4 block (amax, scale, codes) lives in one thread's registers.
-          const int I = N / 2;
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) s_epi_g[jj * kEpiStride + m] = alpha * __uint_as_float(r[jj]);
-          epi_bar(eg);
-          const int jj = et >> 2, blk = et & 3;
-          if (jj < jn) {
-            const float* gp = s_epi_g + jj * kEpiStride + 16 * blk;
-            float h[16];
-            float amax = 0.0f;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              const float g = gp[t];
-              h[t] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), gp[64 + t]);
-              amax = fmaxf(amax, fabsf(h[t]));
-            }
-            float recip;
-            const uint32_t sfb = nvfp4_block_scale(amax, p.h_scale, &recip);
-            const uint32_t lo = nvfp4_codes8(h, recip), hi = nvfp4_codes8(h + 8, recip);
-            const int64_t row = d.x_row + j0 + jj;
-            const int i0 = d.mt * 64 + 16 * blk;
-            *reinterpret_cast<uint2*>(p.h_codes + row * (I / 2) + i0 / 2) = make_uint2(lo, hi);
-            p.h_sf[tiled_sf_offset(row, i0 / 16, I)] = static_cast<uint8_t>(sfb);
-            if (p.h_f32) {
-              float4* dst = reinterpret_cast<float4*>(p.h_f32 + row * I + i0);
-#pragma unroll
-              for (int t = 0; t < 4; ++t) dst[t] = make_float4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
-            }
-          }
-          epi_bar(eg);
+          epi_chunk_silu(r, m, et, eg, jn, alpha, s_epi_g, d.x_row + j0, d.mt * 64, so);
         }
       }
       // with two groups, this group's next unit rewrites the same token table

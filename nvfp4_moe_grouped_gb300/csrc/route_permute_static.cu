@@ -8,8 +8,6 @@
 // point gives them routing and permutation with no workspace argument: its
 // scratch is a fixed array in the library's own device memory, reserved on
 // every GPU that loads the library for as long as the process lives.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace moe {
@@ -21,21 +19,15 @@ constexpr size_t kStaticScratchBytes = 1u << 20;
 
 static __device__ __align__(256) uint8_t g_route_scratch[kStaticScratchBytes];
 
-// Device address of g_route_scratch on the current device, looked up once per
-// device.  Host code must not pass the symbol itself to a kernel: on the host
-// it names a stand-in object, not device memory.
+// Device address of g_route_scratch in the current device's context.  Host
+// code must not pass the symbol itself to a kernel: on the host it names a
+// stand-in object, not device memory.  The lookup allocates nothing and is
+// cheap, so it runs on every call: a cached address could outlive its context
+// (cudaDeviceReset, or another context made current on the same device).
 void* static_scratch_address() {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace
@@ -49,6 +41,10 @@ extern "C" moe_status moe_route_permute_static(const float* logits, int T, int E
                                                float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
                                                int32_t* expanded_to_perm, int32_t* expanded_to_row, void* stream) {
   if (T < 1 || E < 1 || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  // the shape limits of moe_route_permute come first, so an unsupported shape gets the same status here
+  if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  // then the size (before the pointers: a caller's oversized problem is reported as such)
   const size_t need = moe_route_permute_workspace_size(T, E, k);
   if (need > kStaticScratchBytes) return MOE_ERR_WORKSPACE;
   void* scratch = static_scratch_address();

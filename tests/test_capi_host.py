@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.moe_abi_version() == 4
+    assert L.moe_abi_version() == 5
     for s in range(8):
         assert L.moe_status_string(s)
     assert L.moe_status_string(99) == b"unknown status"
@@ -135,8 +135,9 @@ def test_grouped_gemm_rejects_before_launch(L):
 
 
 def test_finalize_and_forward_reject_before_launch(L):
-    assert L.moe_finalize(P, P, P, 4, 2, 12, P, None) == UNSUPPORTED   # N % 8
-    assert L.moe_finalize(Q, P, P, 4, 2, 16, P, None) == MISALIGNED
+    assert L.moe_finalize(P, 8, P, P, 4, 2, 12, P, None) == UNSUPPORTED   # N % 8
+    assert L.moe_finalize(Q, 8, P, P, 4, 2, 16, P, None) == MISALIGNED
+    assert L.moe_finalize(P, 0, P, P, 4, 2, 16, P, None) == INVALID       # no rows of y
     w = _lib.Weights(P, P, P, P)
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 200, 128, 1.0, P, P, 1 << 30, None) == UNSUPPORTED
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 256, 128, 0.0, P, P, 1 << 30, None) == INVALID

@@ -70,5 +70,10 @@ def test_static_scratch_rejects_oversized_problems():
     L = _lib.load()
     T, E, k = 65536, 1024, 8   # needs far more than 1 MiB of scratch
     assert L.moe_route_permute_workspace_size(T, E, k) > L.moe_route_permute_static_scratch_bytes()
-    fake = ctypes.c_void_p(0x1000)
-    assert L.moe_route_permute_static(fake, T, E, k, *([fake] * 6), None) == 7  # MOE_ERR_WORKSPACE
+    # Null pointers everywhere: the size check answers first (MOE_ERR_WORKSPACE).  Were it ever to let
+    # the call through, the null-pointer check behind it would still stop it on the host before any launch.
+    assert L.moe_route_permute_static(None, T, E, k, *([None] * 6), None) == 7  # MOE_ERR_WORKSPACE
+    # shapes the routing kernels do not implement get MOE_ERR_UNSUPPORTED, as from moe_route_permute,
+    # however large their workspace would be
+    assert L.moe_route_permute_static(None, 65536, 2048, 8, *([None] * 6), None) == 3
+    assert L.moe_route_permute_static(None, 65536, 256, 33, *([None] * 6), None) == 3
