@@ -111,9 +111,11 @@ MOE_API moe_status moe_device_error(int32_t* code, int32_t* where);
  * MOE_ERR_TIMEOUT and its kernel returns early. */
 MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
 
-/* Test hook: bit 0 makes the next grouped-GEMM launches skip filling their
+/* Test hooks: bit 0 makes the next grouped-GEMM launches skip filling their
  * first pipeline stage, so the bounded-wait path can be exercised without
- * faulting anything.  0 (the default) for normal operation. */
+ * faulting anything; bit 1 makes them keep the one-CTA 128-row tile where
+ * the CTA-pair tile would run, so both kernels can be compared on one input.
+ * 0 (the default) for normal operation. */
 MOE_API void moe_debug_set_flags(int flags);
 
 /* Bytes of a blocked weight buffer of `rows` rows (rows % 128 == 0) and K
@@ -287,9 +289,13 @@ MOE_API moe_status nvfp4_quantize(const void* x, int in_dtype, int64_t src_rows,
  *   ep            host pointer to epilogue arguments (NULL for NONE)
  *   ws / ws_bytes workspace of moe_grouped_gemm_workspace_size(epilogue, T, k, N)
  *                 bytes (FINALIZE only; 0 otherwise)
- * Tiling: the kernel takes 128 weight rows per tile as the MMA M dimension and
- * up to 64 (decode regime: the allocation implies <= 48 routed rows per
- * expert on average) or 128 (otherwise) routed rows as MMA N.
+ * Tiling: weight rows are the MMA M dimension and routed rows MMA N.  In the
+ * decode regime (the allocation implies <= 48 routed rows per expert on
+ * average) one CTA per SM takes 128 weight rows x up to 64 routed rows per
+ * unit.  Otherwise, where N % 256 == 0, two CTAs of a cluster take 256 weight
+ * rows x up to 192 routed rows per unit with M = 256 (tcgen05 CTA-pair) MMAs
+ * (for FINALIZE, when a 256-column accumulator chunk of T rows fits 64 MiB);
+ * else one CTA takes 128 weight rows x up to 128 routed rows.
  * Requires K % 64 == 0, N % 128 == 0,
  * E <= 1024, a_rows_alloc % 128 == 0, all pointers 16-byte aligned.
  * Device-side errors (read with moe_device_error): expert offsets that would

@@ -702,6 +702,479 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
   }
 }
 
+// ===========================================================================
+// CTA-pair kernel (prefill regime): tcgen05 cta_group::2.
+//
+// Two CTAs of a cluster form a pair that computes one unit = (expert, up to
+// 192 of its routed rows, 256 weight rows) with M = 256 MMAs: CTA r holds
+// weight tile 2*mt2 + r (128 rows, MMA M half r) and routed rows [n/2*r,
+// n/2*(r+1)) of the unit (MMA N half r); one thread of the even CTA issues
+// the MMAs, which read both CTAs' shared memory and write each CTA's
+// accumulator rows into its own tensor memory.  Per SM this doubles the work
+// of one MMA instruction (128 x 192 x 64 against 128 x 128 x 64 for the
+// one-CTA tile) and brings the bytes each SM moves from L2 per FLOP to 0.6 of
+// the one-CTA tile's: a 34 KB stage feeds 12.6 MFLOP per SM where the
+// one-CTA tile's 37 KB stage fed 8.4.
+// Tensor memory of each CTA: two 192-column accumulators (the epilogue of one
+// unit overlaps the mainloop of the next) and three 40-column scale slots, 504
+// of the 512 columns.  The MMA reads weight row r's scales from lane r % 128
+// only (column scale address + r / 32), but every lane quadrant of the
+// accumulator reads the scales of every routed row: those sit in all four
+// quadrants (column scale address + n / 32 holds routed rows 32c..32c+31 in
+// lanes 0-31 of each quadrant).  A slot: 16 columns of weight scales (4 per K
+// step) and 24 of routed-row scales (6 per K step, 192 rows).  A slot is
+// reused three fills later, once the MMAs of that fill have completed (the
+// empty barrier of its stage); the MMA thread waits for each stage's scales on
+// its own, so two stages stay queued in the tensor pipe while the slot of the
+// next one is refilled.
+// Roles per CTA: warps 0 and 10-11 (10-12) issue copies (each CTA its own halves),
+// warp 1 owns tensor memory (in the even CTA its lane 0 issues the MMAs),
+// warps 6-9 stage scales into their own CTA's tensor memory and tell the even
+// CTA, warps 2-5 (and 12-15) drain the accumulator and run the epilogue.
+// Signals between the CTAs: the MMA thread's commits arrive on both CTAs'
+// stage-empty and accumulator-full barriers (one multicast commit each); the
+// staging and epilogue warps of both CTAs arrive on the even CTA's
+// scales-ready and accumulator-empty barriers.
+// ===========================================================================
+constexpr int kPairBN = 192;               // routed rows per pair unit (MMA N)
+constexpr int kPairStages = 5;
+constexpr int kPairSlots = 3;              // tensor-memory scale slots
+constexpr uint32_t kPairSlotCols = 40;     // 16 weight-scale + 24 routed-row-scale columns
+
+// EG = epilogue warp groups.  With two groups, three copy warps (0, 10, 11) keep
+// the CTA at 16 warps (128 registers each); with one, four (0, 10-12).
+template <int EG>
+struct PairCfg {
+  static constexpr int kProducers = EG == 2 ? 3 : 4;
+  static constexpr int kThreads = 32 * (kExtraWarp + (kProducers - 1) + 4 * (EG - 1));
+  static constexpr int kEpi1Warp = kExtraWarp + kProducers - 1;  // first warp of epilogue group 1
+  static constexpr int kXStageBytes = (kPairBN / 2) * (kBK / 2);  // this CTA's half of the routed rows
+  static constexpr int kSfxStageBytes = 2 * kSfStageBytes;        // scales of up to two 128-row blocks
+  static constexpr int kAccBufs = 2;
+  static constexpr uint32_t kSfTmemBase = kAccBufs * kPairBN;
+  static_assert(kSfTmemBase + kPairSlots * kPairSlotCols <= kTmemCols, "tensor memory budget");
+  static_assert(kPairStages >= kProducers, "more producers than stages would alias barrier phases");
+  static constexpr int w = 0;
+  static constexpr int x = w + kPairStages * kWStageBytes;
+  static constexpr int sfx = x + kPairStages * kXStageBytes;
+  static constexpr int epi = sfx + kPairStages * kSfxStageBytes;       // float [EG][32][kEpiStride]
+  static constexpr int tok_t = epi + EG * 32 * kEpiStride * 4;         // int [EG][2][kPairBN]
+  static constexpr int tok_w = tok_t + EG * 2 * kPairBN * 4;           // float [EG][2][kPairBN]
+  static constexpr int bars = tok_w + EG * 2 * kPairBN * 4;            // uint64 [3*S + 2*kAccBufs + 1]
+  static constexpr int misc = bars + (3 * kPairStages + 2 * kAccBufs + 1) * 8;
+  static constexpr int last = misc + 16;                               // int [kProducers][S]
+  static constexpr int info = last + kProducers * kPairStages * 4;     // int [S]
+  static constexpr int sched = info + kPairStages * 4;                 // int [3][kMaxExperts+1]
+  static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
+  static constexpr int smem_bytes = total + 1024;
+  static_assert(smem_bytes <= 232448, "shared memory budget");
+  static_assert(x % 1024 == 0 && kXStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+};
+
+struct PairUnit {
+  int e, nb, mt2, rows, n_mma, x_row, m_off;
+  bool valid;
+};
+
+// Pair unit u -> (column chunk, expert e, 192-row block nb, weight tile pair mt2);
+// the same order as decode_unit with MTC weight tile pairs per chunk.
+MOE_DEVINL PairUnit decode_pair_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E,
+                                     int MTC, int U, int64_t rows_alloc, int64_t items, int& e_hint) {
+  PairUnit d;
+  const int c = u / U;
+  const int uc = u - c * U;
+  if (unit_start[e_hint] > uc) e_hint = 0;
+  d.e = e_hint = find_expert_from(unit_start, E, uc, e_hint);
+  const int local = uc - unit_start[d.e];
+  d.nb = local / MTC;
+  d.mt2 = c * MTC + (local - d.nb * MTC);
+  const int m_e = off[d.e + 1] - off[d.e];
+  d.rows = min(kPairBN, m_e - d.nb * kPairBN);
+  d.n_mma = (d.rows + 31) & ~31;
+  d.x_row = pad_start[d.e] + d.nb * kPairBN;
+  d.m_off = off[d.e] + d.nb * kPairBN;
+  d.valid = d.rows > 0 && d.x_row >= 0 && static_cast<int64_t>(d.x_row) + d.n_mma <= rows_alloc && d.m_off >= 0 &&
+            static_cast<int64_t>(d.m_off) + d.rows <= items;
+  return d;
+}
+
+template <int EG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_x16, const __grid_constant__ CUtensorMap tm_x96,
+                             const GemmParams p) {
+  using C = PairCfg<EG>;
+  constexpr int S = kPairStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_w = smem + C::w;
+  uint8_t* s_x = smem + C::x;
+  uint8_t* s_sfx = smem + C::sfx;
+  float* s_epi = reinterpret_cast<float*>(smem + C::epi);
+  int* s_tok_t = reinterpret_cast<int*>(smem + C::tok_t);
+  float* s_tok_w = reinterpret_cast<float*>(smem + C::tok_w);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bars);
+  uint64_t* empty = full + S;
+  uint64_t* sf_ready = empty + S;
+  uint64_t* acc_full = sf_ready + S;
+  uint64_t* acc_empty = acc_full + C::kAccBufs;
+  uint64_t* mma_done = acc_empty + C::kAccBufs;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::misc + 4);
+  int* s_info = reinterpret_cast<int*>(smem + C::info);
+  int* unit_start = reinterpret_cast<int*>(smem + C::sched);
+  int* pad_start = unit_start + (kMaxExperts + 1);
+  int* off = pad_start + (kMaxExperts + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(cluster_id_x()), npairs = static_cast<int>(cluster_count_x());
+  const int E = p.E, N = p.N, K = p.K;
+  const int MT = N / kBM;
+  const int MTC = p.mt_chunk;  // weight tile pairs per column chunk
+  const int KT = (K + kBK - 1) / kBK;
+
+  // ---- prologue ----------------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&sf_ready[s], 8); }
+    for (int b = 0; b < C::kAccBufs; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 8); }
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {  // the pair's tensor memory: one warp of each CTA allocates together
+    tmem_alloc_pair(s_tmem, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = lane * per;
+    int units = 0, pads = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      const int m = __ldg(p.expert_offsets + e + 1) - __ldg(p.expert_offsets + e);
+      units += ((m + kPairBN - 1) / kPairBN) * MTC;
+      pads += ((m + 127) / 128) * 128;
+    }
+    int iu = units, ip = pads;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yu = __shfl_up_sync(0xffffffffu, iu, o), yp = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) { iu += yu; ip += yp; }
+    }
+    int ru = iu - units, rp = ip - pads;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      const int o0 = __ldg(p.expert_offsets + e), o1 = __ldg(p.expert_offsets + e + 1);
+      unit_start[e] = ru;
+      pad_start[e] = rp;
+      off[e] = o0;
+      ru += ((o1 - o0 + kPairBN - 1) / kPairBN) * MTC;
+      rp += ((o1 - o0 + 127) / 128) * 128;
+    }
+    if (lane == 31) {
+      unit_start[E] = iu;
+      pad_start[E] = ip;
+      off[E] = __ldg(p.expert_offsets + E);
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs: barriers initialised, tensor memory allocated, schedule built
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const int U = unit_start[E];
+  const int total_units = U * ((MT / 2) / MTC);
+
+  if (warp == 0 || (warp >= kExtraWarp && warp < kExtraWarp + C::kProducers - 1)) {
+    // ---------------- producers (each CTA loads its own halves) ----------------
+    const int pid = warp == 0 ? 0 : warp - kExtraWarp + 1;
+    int* s_last = reinterpret_cast<int*>(smem + C::last);
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int fill = 0;
+      for (int s = 0; s < S; ++s) s_last[pid * S + s] = -1;
+      bool skip_once = pid == 0 && (p.debug_flags & 1) != 0;
+      int e_hint = 0;
+      bool ok = true;
+      for (int u = pair; ok && u < total_units; u += npairs) {
+        const PairUnit d = decode_pair_unit(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, p.items, e_hint);
+        if (!d.valid) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+          *s_abort = 1;
+          break;
+        }
+        const int mt = 2 * d.mt2 + static_cast<int>(rank);
+        const uint8_t* w_src = p.w_blocked + static_cast<int64_t>(d.e * MT + mt) * KT * kWStageBytes;
+        const int half = d.n_mma / 2;
+        const int xr = d.x_row + static_cast<int>(rank) * half;
+        const int b0 = d.x_row >> 7, b1 = (d.x_row + d.n_mma - 1) >> 7;
+        const uint8_t* sf0 = p.x_sf + static_cast<int64_t>(b0) * (K / 64) * 512;
+        for (int kt = 0; kt < KT; ++kt, ++fill) {
+          if (fill % C::kProducers == pid) {
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, s_abort)) {
+              if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 11);
+              *s_abort = 1;
+              ok = false;
+              break;
+            }
+            const int steps = min(4, (K - kt * kBK) / 64);
+            if (skip_once) {
+              skip_once = false;
+            } else {
+              const uint32_t bytes = kWStageBytes + half * (kBK / 2) + (b1 > b0 ? 2 : 1) * steps * 512;
+              mbar_arrive_expect_tx(&full[stage], bytes);
+              bulk_load(s_w + stage * kWStageBytes, w_src + static_cast<int64_t>(kt) * kWStageBytes, kWStageBytes,
+                        &full[stage], pol_w);
+              uint8_t* xdst = s_x + stage * C::kXStageBytes;
+              if (half == kPairBN / 2) {
+                tma_load_2d(xdst, &tm_x96, &full[stage], kt * (kBK / 2), xr, pol_x);
+              } else {
+                for (int q = 0; q < half / 16; ++q)
+                  tma_load_2d(xdst + q * 16 * (kBK / 2), &tm_x16, &full[stage], kt * (kBK / 2), xr + 16 * q, pol_x);
+              }
+              uint8_t* sdst = s_sfx + stage * C::kSfxStageBytes;
+              bulk_load(sdst, sf0 + kt * 4 * 512, steps * 512, &full[stage], pol_x);
+              if (b1 > b0)
+                bulk_load(sdst + kSfStageBytes, sf0 + static_cast<int64_t>(K / 64) * 512 + kt * 4 * 512, steps * 512,
+                          &full[stage], pol_x);
+              s_last[pid * S + stage] = fill;
+            }
+          }
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+    __syncwarp();
+    asm volatile("bar.sync 2, %0;" ::"r"(C::kProducers * 32) : "memory");
+    if (pid == 0 && lane == 0) {
+      int zero = 0;
+      for (int s = 0; s < S; ++s) {
+        int last = -1;
+        for (int q = 0; q < C::kProducers; ++q) last = max(last, s_last[q * S + s]);
+        if (last >= 0)
+          mbar_wait_bounded(&full[s], static_cast<uint32_t>(last / S) & 1u, p.timeout_ns,
+                            reinterpret_cast<volatile int*>(&zero));
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (even CTA, one thread) ----------------
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fill = 0;
+      int acc_i = 0;
+      bool ok = true;
+      const uint64_t adesc0 = smem_desc(smem_u32(s_w), 16, 1024, 2);
+      const uint64_t bdesc0 = smem_desc(smem_u32(s_x), 16, 1024, 2);
+      for (int u = pair; ok && u < total_units; u += npairs, ++acc_i) {
+        const int b = acc_i % C::kAccBufs;
+        if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 12);
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * kPairBN;
+        uint32_t idesc = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+          // both CTAs staged this stage's scales: their copies of the stage have landed too
+          if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
+            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 13);
+            *s_abort = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (kt == 0) idesc = idesc_mxf4nvf4(s_info[stage], 256);
+          const uint32_t sf_col = tmem_base + C::kSfTmemBase + (fill % kPairSlots) * kPairSlotCols;
+          const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * kWStageBytes) >> 4);
+          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * C::kXStageBytes) >> 4);
+          if (kt * kBK + kBK <= K) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g,
+                                (kt | g) != 0);
+          } else {
+            const int steps = (K - kt * kBK) / 64;
+            for (int g = 0; g < steps; ++g)
+              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g,
+                                (kt | g) != 0);
+          }
+          mma_commit_pair(&empty[stage], 0x3);
+          ++fill;
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit_pair(&acc_full[b], 0x3);
+      }
+      mma_commit_pair(mma_done, 0x3);
+      int zero = 0;
+      mbar_wait_bounded(mma_done, 0, p.timeout_ns, reinterpret_cast<volatile int*>(&zero));
+    }
+  } else if (warp >= 6 && warp < kExtraWarp) {
+    // ---------------- scale staging warps 6..9 (each CTA its own tensor memory) ----------------
+    // Per fill, the 40 columns of the fill's slot in this warp's lane quadrant:
+    // columns 4g..4g+3 the weight scales of K step g (only this quadrant's own
+    // column is read by the MMA: weight row r's scales come from quadrant r/32),
+    // columns 16+6g..16+6g+5 the routed-row scales of K step g, column c holding
+    // routed rows 32c..32c+31 of the unit in lanes 0-31 of every quadrant.
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const uint32_t quad_lane = (32u * quad) << 16;
+    const uint32_t sf_ready_even = map_shared_rank(smem_u32(sf_ready), 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    int fill = 0;
+    int e_hint = 0;
+    bool ok = true;
+    for (int u = pair; ok && u < total_units; u += npairs) {
+      const PairUnit d = decode_pair_unit(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, p.items, e_hint);
+      if (!d.valid) {
+        if (lane == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+          *s_abort = 1;
+        }
+        break;
+      }
+      // the unit starts 0 or 64 rows into a 128-row scale block: routed row 32c of the unit is
+      // column (o + c) % 4 of block (o + c) / 4, o = (x_row % 128) / 32
+      const bool mid = (d.x_row & 127) != 0;
+      for (int kt = 0; kt < KT; ++kt, ++fill) {
+        bool got = mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort);
+        if (got && fill >= kPairSlots) {
+          // the slot's previous fill (fill - kPairSlots) must be consumed by its MMAs
+          const int pf = fill - kPairSlots;
+          got = mbar_wait_bounded(&empty[pf % S], static_cast<uint32_t>(pf / S) & 1u, p.timeout_ns, s_abort);
+        }
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) {
+            if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 14);
+            *s_abort = 1;
+          }
+          ok = false;
+          break;
+        }
+        const uint8_t* sfw = s_w + stage * kWStageBytes + 16384 + lane * 16 + 4 * quad;
+        const uint8_t* sfx = s_sfx + stage * C::kSfxStageBytes + lane * 16;
+        uint32_t v[40];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t a = *reinterpret_cast<const uint32_t*>(sfw + 512 * g);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[4 * g + j] = (static_cast<uint32_t>(j) == quad) ? a : 0u;
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sfx + 512 * g);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sfx + kSfStageBytes + 512 * g);
+          v[16 + 6 * g + 0] = mid ? b0.z : b0.x;
+          v[16 + 6 * g + 1] = mid ? b0.w : b0.y;
+          v[16 + 6 * g + 2] = mid ? b1.x : b0.z;
+          v[16 + 6 * g + 3] = mid ? b1.y : b0.w;
+          v[16 + 6 * g + 4] = mid ? b1.z : b1.x;
+          v[16 + 6 * g + 5] = mid ? b1.w : b1.y;
+        }
+        const uint32_t slot = tmem_base + quad_lane + C::kSfTmemBase + (fill % kPairSlots) * kPairSlotCols;
+        tmem_st_32cols(slot, *reinterpret_cast<const uint32_t(*)[32]>(v));
+        tmem_st_8cols(slot + 32, v + 32);
+        tmem_st_wait();
+        tc_fence_before();
+        if (kt == 0 && warp == 6 && lane == 0) s_info[stage] = d.n_mma;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(sf_ready_even + stage * 8);
+        if (++stage == S) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 (and 12..15) ----------------
+    const int q = warp & 3;
+    const int m = 32 * q + lane;
+    const int eg = warp >= C::kEpi1Warp ? 1 : 0;
+    const int et = eg ? threadIdx.x - 32 * C::kEpi1Warp : threadIdx.x - 64;
+    float* s_epi_g = s_epi + eg * 32 * kEpiStride;
+    const uint32_t acc_empty_even = map_shared_rank(smem_u32(acc_empty), 0);
+    const float x_scale = __ldg(p.x_scale);
+    if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && eg == 0 && et == 0)
+      *p.h_scale_out = p.h_scale;
+    const SiluOut so{p.h_scale, p.h_codes, p.h_sf, p.h_f32, N / 2};
+    int acc_i = 0;
+    int e_hint = 0;
+    for (int u = pair; u < total_units; u += npairs, ++acc_i) {
+      const PairUnit d = decode_pair_unit(u, unit_start, pad_start, off, E, MTC, U, p.rows_alloc, p.items, e_hint);
+      if (!d.valid) {
+        if (et == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_INVALID_ARG, 5);
+          *s_abort = 1;
+        }
+        break;
+      }
+      if (acc_i % EG != eg) continue;
+      const int b = acc_i % C::kAccBufs;
+      const bool got = mbar_wait_bounded(&acc_full[b], (acc_i / C::kAccBufs) & 1, p.timeout_ns, s_abort);
+      if (epi_any(eg, !got)) {
+        if (et == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 15);
+          *s_abort = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const int mt = 2 * d.mt2 + static_cast<int>(rank);
+      const float alpha = x_scale * __ldg(p.w_scale + d.e);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kPairBN;
+      // token table double-buffered per group: this group's unit before last read the other half
+      int* tok_tab = s_tok_t + (eg * 2 + ((acc_i / EG) & 1)) * kPairBN;
+      float* w_tab = s_tok_w + (eg * 2 + ((acc_i / EG) & 1)) * kPairBN;
+      if (p.epilogue == MOE_EPI_FINALIZE) {
+        for (int i = et; i < d.rows; i += 128) {
+          const int ex = __ldg(p.perm_to_expanded + d.m_off + i);
+          const bool in_range = ex >= 0 && ex < p.T * p.k;
+          if (!in_range) record_error(p.err, MOE_ERR_INVALID_ARG, 6);
+          tok_tab[i] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
+          w_tab[i] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
+        }
+        epi_bar(eg);
+      }
+      for (int j0 = 0; j0 < d.rows; j0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32cols(taddr + j0, r);
+        tmem_ld_wait();
+        if (j0 + 32 >= d.rows) {
+          // the accumulator is fully read: hand it back to the MMA thread before the last chunk's math
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_even + b * 8);
+        }
+        const int jn = min(32, d.rows - j0);
+        if (p.epilogue == MOE_EPI_NONE) {
+          epi_chunk_none(r, jn, d.x_row + j0, static_cast<int64_t>(mt) * kBM + m, N, alpha,
+                         static_cast<uint16_t*>(p.out));
+        } else if (p.epilogue == MOE_EPI_FINALIZE) {
+          epi_chunk_finalize(r, lane, jn, tok_tab + j0, w_tab + j0,
+                             static_cast<float*>(p.out) + static_cast<int64_t>(mt) * kBM + 32 * q + 4 * (lane >> 2),
+                             N, p.fin_gather != 0);
+        } else {
+          epi_chunk_silu(r, m, et, eg, jn, alpha, s_epi_g, d.x_row + j0, mt * 64, so);
+        }
+      }
+    }
+  }
+  // (control reaches here on every path)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (!leader && lane == 0) {
+      // the even CTA's MMAs write this CTA's tensor memory: wait for the last of them
+      int zero = 0;
+      mbar_wait_bounded(mma_done, 0, p.timeout_ns, reinterpret_cast<volatile int*>(&zero));
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // neither CTA frees its tensor memory or exits while the pair may still use it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -742,6 +1215,59 @@ moe_status launch_gemm(const CUtensorMap& tm_x, const CUtensorMap& tm_xt, const 
   if (max_units < grid) grid = static_cast<int>(max_units);
   grouped_gemm_kernel<BN, EG><<<grid, C::kThreads, C::smem_bytes, st>>>(tm_x, tm_xt, p);
   return check_launch();
+}
+
+template <int EG>
+moe_status prepare_pair() {
+  return cudaFuncSetAttribute(grouped_gemm_pair_kernel<EG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PairCfg<EG>::smem_bytes) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_RESOURCE;
+}
+
+// CTA pairs the current device can hold at once with this configuration (each CTA
+// takes a whole SM's shared memory); looked up once per device.
+template <int EG>
+int resident_pairs() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 1024, 1, 1);
+  cfg.blockDim = dim3(PairCfg<EG>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<EG>::smem_bytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EG>, &cfg) != cudaSuccess) return 0;
+  cached[dev] = n;
+  return n;
+}
+
+template <int EG>
+moe_status launch_pair(const CUtensorMap& tm16, const CUtensorMap& tm96, const GemmParams& p, int64_t max_units,
+                       cudaStream_t st) {
+  int pairs = resident_pairs<EG>();
+  if (pairs < 1) return MOE_ERR_RESOURCE;
+  if (max_units < pairs) pairs = static_cast<int>(max_units);
+  grouped_gemm_pair_kernel<EG><<<2 * pairs, PairCfg<EG>::kThreads, PairCfg<EG>::smem_bytes, st>>>(tm16, tm96, p);
+  return check_launch();
+}
+
+// FINALIZE column chunk of the pair kernel, in weight tile pairs: the largest
+// divisor of N/256 whose live accumulator (T x 256*chunk floats) stays within
+// kFinalizeAtomicMaxBytes; 0 if not even one pair fits.
+int finalize_pair_chunk(int T, int N) {
+  const int MT2 = N / 256;
+  for (int c = MT2; c >= 1; --c)
+    if (MT2 % c == 0 && static_cast<int64_t>(T) * c * 256 * 4 <= kFinalizeAtomicMaxBytes) return c;
+  return 0;
 }
 
 }  // namespace
@@ -826,7 +1352,6 @@ moe_status grouped_gemm_enqueue(const uint8_t* a_codes, const uint8_t* a_sf, con
     p.fin_gather = finalize_gathers(ep->T, N) ? 1 : 0;
     if (!p.fin_gather) p.mt_chunk = finalize_mt_chunk(ep->T, N);
   }
-  if (p.mt_chunk == 0) p.mt_chunk = N / kBM;
   p.rows_alloc = a_rows_alloc;
   p.items = epilogue == MOE_EPI_FINALIZE ? static_cast<int64_t>(ep->T) * ep->k : INT64_MAX;
   p.err = device_error_word();
@@ -835,24 +1360,40 @@ moe_status grouped_gemm_enqueue(const uint8_t* a_codes, const uint8_t* a_sf, con
   if (!p.err) return MOE_ERR_CUDA;
 
   const int bn = gemm_tile_rows(a_rows_alloc, E);
+  // The prefill regime runs on CTA pairs (256 weight rows x up to 192 routed rows per unit) where N is a
+  // multiple of 256 and, for FINALIZE, a 256-column accumulator chunk stays within the atomic budget.
+  // Debug flag bit 1 keeps the one-CTA 128-row tile (so tests can compare both kernels on one input).
+  bool pair = bn == 128 && N % 256 == 0 && (p.debug_flags & 2) == 0;
+  if (pair && epilogue == MOE_EPI_FINALIZE && finalize_pair_chunk(ep->T, N) == 0) pair = false;
+  if (pair) p.mt_chunk = epilogue == MOE_EPI_FINALIZE ? finalize_pair_chunk(ep->T, N) : N / 256;
+  else if (p.mt_chunk == 0) p.mt_chunk = N / kBM;
   // two epilogue groups pay off where FINALIZE outlasts the mainloop (128-row tiles); at decode the
   // weight stream dominates and four copy warps are worth more (measured: 0.303 vs 0.319 ms, C4 down)
   const bool two_groups = bn == 128 && epilogue == MOE_EPI_FINALIZE;
-  const int64_t max_units = ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
+  const int64_t max_units = pair ? ((a_rows_alloc + kPairBN - 1) / kPairBN) * (N / 256)
+                                 : ((a_rows_alloc + bn - 1) / bn) * (N / kBM);
   if (max_units > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
-  // routed-row tiles come as 32-row boxes, or as one box when a unit fills the whole tile
+  // routed-row tiles come as 32-row boxes, or as one box when a unit fills the whole tile (one-CTA
+  // kernel); as 16-row boxes or one 96-row box per CTA (pair kernel)
   CUtensorMap tm_x, tm_xt;
-  if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, 32)) return MOE_ERR_CUDA;
-  if (!make_code_map(&tm_xt, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, bn)) return MOE_ERR_CUDA;
+  if (!make_code_map(&tm_x, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, pair ? 16 : 32))
+    return MOE_ERR_CUDA;
+  if (!make_code_map(&tm_xt, a_codes, static_cast<uint64_t>(a_rows_alloc), K / 2, pair ? kPairBN / 2 : bn))
+    return MOE_ERR_CUDA;
   {
-    const moe_status ps = bn == 64 ? prepare_gemm<64, 1>() : two_groups ? prepare_gemm<128, 2>() : prepare_gemm<128, 1>();
+    const moe_status ps = pair ? (epilogue == MOE_EPI_NONE ? prepare_pair<1>() : prepare_pair<2>())
+                          : bn == 64 ? prepare_gemm<64, 1>()
+                          : two_groups ? prepare_gemm<128, 2>()
+                                       : prepare_gemm<128, 1>();
     if (ps != MOE_OK) return ps;
   }
   if (clear_accumulator && epilogue == MOE_EPI_FINALIZE && !p.fin_gather) {
     if (cudaMemsetAsync(ws, 0, static_cast<size_t>(ep->T) * N * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  moe_status s = bn == 64       ? launch_gemm<64, 1>(tm_x, tm_xt, p, max_units, st)
+  moe_status s = pair ? (epilogue == MOE_EPI_NONE ? launch_pair<1>(tm_x, tm_xt, p, max_units, st)
+                                                  : launch_pair<2>(tm_x, tm_xt, p, max_units, st))
+                 : bn == 64  ? launch_gemm<64, 1>(tm_x, tm_xt, p, max_units, st)
                  : two_groups ? launch_gemm<128, 2>(tm_x, tm_xt, p, max_units, st)
                               : launch_gemm<128, 1>(tm_x, tm_xt, p, max_units, st);
   if (s != MOE_OK) return s;

@@ -644,3 +644,13 @@ def test_forward_graph_replays_the_layer(stage_events):
     assert np.linalg.norm(a - b) / np.linalg.norm(b) < 1e-3
     g.close()
     assert moe.device_error() == (0, 0)
+
+
+def test_fp4_mma_probes_run_and_report_rates():
+    """Both dense FP4 MMA-rate probes (one CTA per SM, M = 128; CTA pairs, M = 256) finish without a device
+    error and report a rate in the range a GB300's tensor cores can give."""
+    one = moe.fp4_mma_peak_tflops(iters=2000, reps=2)
+    pair = moe.fp4_mma_peak_tflops(iters=2000, reps=2, pair=True)
+    assert moe.device_error() == (0, 0)
+    for rate in (one, pair):
+        assert 1000.0 < rate < 20000.0, (one, pair)
