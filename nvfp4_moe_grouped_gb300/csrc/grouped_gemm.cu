@@ -737,7 +737,9 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
 // scales-ready and accumulator-empty barriers.
 // ===========================================================================
 constexpr int kPairBN = 192;               // routed rows per pair unit (MMA N)
-constexpr int kPairStages = 5;
+constexpr int kPairStages = 6;
+constexpr int kPairMaxExperts = 512;       // larger launches take the one-CTA kernel
+constexpr int kPairEpiRows = 16;           // routed rows per SiLU staging round
 constexpr int kPairSlots = 3;              // tensor-memory scale slots
 constexpr uint32_t kPairSlotCols = 40;     // 16 weight-scale + 24 routed-row-scale columns
 
@@ -757,15 +759,19 @@ struct PairCfg {
   static constexpr int w = 0;
   static constexpr int x = w + kPairStages * kWStageBytes;
   static constexpr int sfx = x + kPairStages * kXStageBytes;
-  static constexpr int epi = sfx + kPairStages * kSfxStageBytes;       // float [EG][32][kEpiStride]
-  static constexpr int tok_t = epi + EG * 32 * kEpiStride * 4;         // int [EG][2][kPairBN]
-  static constexpr int tok_w = tok_t + EG * 2 * kPairBN * 4;           // float [EG][2][kPairBN]
-  static constexpr int bars = tok_w + EG * 2 * kPairBN * 4;            // uint64 [3*S + 2*kAccBufs + 1]
+  // SiLU staging, float [EG][kPairEpiRows][kEpiStride]; a FINALIZE launch (which stages nothing) keeps
+  // its token tables in the same bytes: int [EG][2][kPairBN] then float [EG][2][kPairBN]
+  static constexpr int epi = sfx + kPairStages * kSfxStageBytes;
+  static constexpr int epi_bytes = EG * kPairEpiRows * kEpiStride * 4;
+  static constexpr int tok_t = epi;
+  static constexpr int tok_w = tok_t + EG * 2 * kPairBN * 4;
+  static_assert(EG * 2 * kPairBN * 8 <= epi_bytes, "token tables fit the staging bytes");
+  static constexpr int bars = epi + epi_bytes;                         // uint64 [3*S + 2*kAccBufs + 1]
   static constexpr int misc = bars + (3 * kPairStages + 2 * kAccBufs + 1) * 8;
   static constexpr int last = misc + 16;                               // int [kProducers][S]
   static constexpr int info = last + kProducers * kPairStages * 4;     // int [S]
-  static constexpr int sched = info + kPairStages * 4;                 // int [3][kMaxExperts+1]
-  static constexpr int total = sched + 3 * (kMaxExperts + 1) * 4;
+  static constexpr int sched = info + kPairStages * 4;                 // int [2][kPairMaxExperts+1]
+  static constexpr int total = sched + 2 * (kPairMaxExperts + 1) * 4;
   static constexpr int smem_bytes = total + 1024;
   static_assert(smem_bytes <= 232448, "shared memory budget");
   static_assert(x % 1024 == 0 && kXStageBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -778,7 +784,7 @@ struct PairUnit {
 
 // Pair unit u -> (column chunk, expert e, 192-row block nb, weight tile pair mt2);
 // the same order as decode_unit with MTC weight tile pairs per chunk.
-MOE_DEVINL PairUnit decode_pair_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E,
+MOE_DEVINL PairUnit decode_pair_unit(int u, const int* unit_start, const int* pad_start, const int32_t* off, int E,
                                      int MTC, int U, int64_t rows_alloc, int64_t items, int& e_hint) {
   PairUnit d;
   const int c = u / U;
@@ -788,14 +794,52 @@ MOE_DEVINL PairUnit decode_pair_unit(int u, const int* unit_start, const int* pa
   const int local = uc - unit_start[d.e];
   d.nb = local / MTC;
   d.mt2 = c * MTC + (local - d.nb * MTC);
-  const int m_e = off[d.e + 1] - off[d.e];
+  const int o0 = __ldg(off + d.e);  // expert offsets straight from global memory (L1-cached)
+  const int m_e = __ldg(off + d.e + 1) - o0;
   d.rows = min(kPairBN, m_e - d.nb * kPairBN);
   d.n_mma = (d.rows + 31) & ~31;
   d.x_row = pad_start[d.e] + d.nb * kPairBN;
-  d.m_off = off[d.e] + d.nb * kPairBN;
+  d.m_off = o0 + d.nb * kPairBN;
   d.valid = d.rows > 0 && d.x_row >= 0 && static_cast<int64_t>(d.x_row) + d.n_mma <= rows_alloc && d.m_off >= 0 &&
             static_cast<int64_t>(d.m_off) + d.rows <= items;
   return d;
+}
+
+// epi_chunk_silu through a 16-row staging buffer: the chunk's 32 routed rows in
+// two rounds of 16 (threads et < 64 compute in each round).
+MOE_DEVINL void epi_chunk_silu16(const uint32_t (&r)[32], int m, int et, int eg, int jn, float alpha, float* s_epi_g,
+                                 int64_t row0, int i_tile, const SiluOut& o) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) s_epi_g[jj * kEpiStride + m] = alpha * __uint_as_float(r[16 * half + jj]);
+    epi_bar(eg);
+    const int jj = et >> 2, blk = et & 3;
+    if (et < 64 && 16 * half + jj < jn) {
+      const float* gp = s_epi_g + jj * kEpiStride + 16 * blk;
+      float h[16];
+      float amax = 0.0f;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const float g = gp[t];
+        h[t] = __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), gp[64 + t]);
+        amax = fmaxf(amax, fabsf(h[t]));
+      }
+      float recip;
+      const uint32_t sfb = nvfp4_block_scale(amax, o.h_scale, &recip);
+      const uint32_t lo = nvfp4_codes8(h, recip), hi = nvfp4_codes8(h + 8, recip);
+      const int64_t row = row0 + 16 * half + jj;
+      const int i0 = i_tile + 16 * blk;
+      *reinterpret_cast<uint2*>(o.h_codes + row * (o.I / 2) + i0 / 2) = make_uint2(lo, hi);
+      o.h_sf[tiled_sf_offset(row, i0 / 16, o.I)] = static_cast<uint8_t>(sfb);
+      if (o.h_f32) {
+        float4* dst = reinterpret_cast<float4*>(o.h_f32 + row * o.I + i0);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) dst[t] = make_float4(h[4 * t], h[4 * t + 1], h[4 * t + 2], h[4 * t + 3]);
+      }
+    }
+    epi_bar(eg);
+  }
 }
 
 template <int EG>
@@ -822,8 +866,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::misc + 4);
   int* s_info = reinterpret_cast<int*>(smem + C::info);
   int* unit_start = reinterpret_cast<int*>(smem + C::sched);
-  int* pad_start = unit_start + (kMaxExperts + 1);
-  int* off = pad_start + (kMaxExperts + 1);
+  int* pad_start = unit_start + (kPairMaxExperts + 1);
+  const int32_t* off = p.expert_offsets;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -866,14 +910,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
       const int o0 = __ldg(p.expert_offsets + e), o1 = __ldg(p.expert_offsets + e + 1);
       unit_start[e] = ru;
       pad_start[e] = rp;
-      off[e] = o0;
       ru += ((o1 - o0 + kPairBN - 1) / kPairBN) * MTC;
       rp += ((o1 - o0 + 127) / 128) * 128;
     }
     if (lane == 31) {
       unit_start[E] = iu;
       pad_start[E] = ip;
-      off[E] = __ldg(p.expert_offsets + E);
     }
   }
   tc_fence_before();
@@ -959,14 +1001,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (even CTA, one thread) ----------------
+    // This one thread issues every MMA of the pair, and the tensor core finishes a
+    // stage's four MMAs in about the time a few dozen instructions take to issue
+    // here: the loop carries the stage's descriptor offsets and scale slot as
+    // running values (no multiplies or divisions), takes the wait's fast path
+    // inline, and issues the first K stage of a unit (which starts the
+    // accumulator) and a partial last stage outside the main loop.
     if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int fill = 0;
       int acc_i = 0;
       bool ok = true;
       const uint64_t adesc0 = smem_desc(smem_u32(s_w), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(s_x), 16, 1024, 2);
+      constexpr uint32_t kAStep = kWStageBytes >> 4, kBStep = C::kXStageBytes >> 4;  // descriptor units per stage
+      uint32_t ab_off = 0;  // stage * kAStep in the low half, stage * kBStep in the high half
+      const uint32_t sf_base = tmem_base + C::kSfTmemBase;
+      uint32_t sf_col = sf_base;
+      const int KF = K / kBK;                      // full 256-element K stages
+      const int k_tail = (K - KF * kBK) / 64;      // MMAs of a partial last stage (0-3)
       for (int u = pair; ok && u < total_units; u += npairs, ++acc_i) {
         const int b = acc_i % C::kAccBufs;
         if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
@@ -977,33 +1030,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kPairBN;
         uint32_t idesc = 0;
-        for (int kt = 0; kt < KT; ++kt) {
+        for (int kt = 0; kt < KF + (k_tail > 0 ? 1 : 0); ++kt) {
           // both CTAs staged this stage's scales: their copies of the stage have landed too
-          if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
+          if (!mbar_try_wait(&sf_ready[stage], phase) &&
+              !mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 13);
             *s_abort = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          if (kt == 0) idesc = idesc_mxf4nvf4(s_info[stage], 256);
-          const uint32_t sf_col = tmem_base + C::kSfTmemBase + (fill % kPairSlots) * kPairSlotCols;
-          const uint64_t adesc = adesc0 + static_cast<uint64_t>((stage * kWStageBytes) >> 4);
-          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((stage * C::kXStageBytes) >> 4);
-          if (kt * kBK + kBK <= K) {
+          const uint64_t adesc = adesc0 + (ab_off & 0xFFFFu);
+          const uint64_t bdesc = bdesc0 + (ab_off >> 16);
+          if (kt == 0) {
+            idesc = idesc_mxf4nvf4(s_info[stage], 256);
+            mma_mxf4nvf4_pair(d_tmem, adesc, bdesc, idesc, sf_col, sf_col + 16, 0u);
+            const int n = kt < KF ? 4 : k_tail;
+            for (int g = 1; g < n; ++g)
+              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g, 1u);
+          } else if (kt < KF) {
 #pragma unroll
             for (int g = 0; g < 4; ++g)
-              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g,
-                                (kt | g) != 0);
+              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g, 1u);
           } else {
-            const int steps = (K - kt * kBK) / 64;
-            for (int g = 0; g < steps; ++g)
-              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g,
-                                (kt | g) != 0);
+            for (int g = 0; g < k_tail; ++g)
+              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g, 1u);
           }
           mma_commit_pair(&empty[stage], 0x3);
-          ++fill;
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+          sf_col += kPairSlotCols;
+          if (sf_col == sf_base + kPairSlots * kPairSlotCols) sf_col = sf_base;
+          ab_off += kAStep | (kBStep << 16);
+          if (++stage == S) { stage = 0; phase ^= 1u; ab_off = 0; }
         }
         if (!ok) break;
         mma_commit_pair(&acc_full[b], 0x3);
@@ -1088,7 +1145,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
     const int m = 32 * q + lane;
     const int eg = warp >= C::kEpi1Warp ? 1 : 0;
     const int et = eg ? threadIdx.x - 32 * C::kEpi1Warp : threadIdx.x - 64;
-    float* s_epi_g = s_epi + eg * 32 * kEpiStride;
+    float* s_epi_g = s_epi + eg * kPairEpiRows * kEpiStride;
     const uint32_t acc_empty_even = map_shared_rank(smem_u32(acc_empty), 0);
     const float x_scale = __ldg(p.x_scale);
     if (p.epilogue == MOE_EPI_SILU_MUL_QUANT && p.h_scale_out && blockIdx.x == 0 && eg == 0 && et == 0)
@@ -1151,7 +1208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
                              static_cast<float*>(p.out) + static_cast<int64_t>(mt) * kBM + 32 * q + 4 * (lane >> 2),
                              N, p.fin_gather != 0);
         } else {
-          epi_chunk_silu(r, m, et, eg, jn, alpha, s_epi_g, d.x_row + j0, mt * 64, so);
+          epi_chunk_silu16(r, m, et, eg, jn, alpha, s_epi_g, d.x_row + j0, mt * 64, so);
         }
       }
     }
@@ -1363,7 +1420,7 @@ moe_status grouped_gemm_enqueue(const uint8_t* a_codes, const uint8_t* a_sf, con
   // The prefill regime runs on CTA pairs (256 weight rows x up to 192 routed rows per unit) where N is a
   // multiple of 256 and, for FINALIZE, a 256-column accumulator chunk stays within the atomic budget.
   // Debug flag bit 1 keeps the one-CTA 128-row tile (so tests can compare both kernels on one input).
-  bool pair = bn == 128 && N % 256 == 0 && (p.debug_flags & 2) == 0;
+  bool pair = bn == 128 && N % 256 == 0 && E <= kPairMaxExperts && (p.debug_flags & 2) == 0;
   if (pair && epilogue == MOE_EPI_FINALIZE && finalize_pair_chunk(ep->T, N) == 0) pair = false;
   if (pair) p.mt_chunk = epilogue == MOE_EPI_FINALIZE ? finalize_pair_chunk(ep->T, N) : N / 256;
   else if (p.mt_chunk == 0) p.mt_chunk = N / kBM;
