@@ -203,6 +203,34 @@ MOE_DEVINL bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeo
   }
 }
 
+// Non-blocking test of the phase with the given parity (the thread is never suspended).
+MOE_DEVINL bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait_bounded by spinning on test_wait: for a thread whose wake-up latency
+// is on the critical path (a suspended try_wait can resume well after the phase
+// completes).  Same bound and abort as mbar_wait_bounded.
+MOE_DEVINL bool mbar_spin_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, volatile int* abort) {
+  if (mbar_test_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA and bulk copies (global -> shared, completion on an mbarrier)
 // ----------------------------------------------------------------------------
@@ -318,6 +346,10 @@ MOE_DEVINL void tmem_st_16cols(uint32_t taddr, const uint32_t* r) {
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+// Each thread of the warp stores one 32-bit column of its lane.
+MOE_DEVINL void tmem_st_1col(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
 // Each thread of the warp stores 8 consecutive 32-bit columns of its lane.
 MOE_DEVINL void tmem_st_8cols(uint32_t taddr, const uint32_t* r) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
@@ -431,6 +463,21 @@ MOE_DEVINL void mma_mxf4nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_d
       "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+// mma_mxf4nvf4_pair with the descriptors given as 32-bit halves: the high halves
+// (stride, version, layout) are fixed for a kernel, so the issuing thread moves
+// only the low halves (start addresses) and never does 64-bit arithmetic.
+MOE_DEVINL void mma_mxf4nvf4_pair_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
+                                     uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %2};\n\t"
+      "mov.b64 bd, {%3, %4};\n\t"
+      "setp.ne.b32 p, %8, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], ad, bd, %5, [%6], [%7], p;\n\t}" ::"r"(
+          d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 // Arrives once on the mbarrier at the same shared-memory offset in each CTA of

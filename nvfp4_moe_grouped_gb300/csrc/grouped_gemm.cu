@@ -748,8 +748,9 @@ constexpr uint32_t kPairSlotCols = 40;     // 16 weight-scale + 24 routed-row-sc
 template <int EG>
 struct PairCfg {
   static constexpr int kProducers = EG == 2 ? 3 : 4;
-  static constexpr int kThreads = 32 * (kExtraWarp + (kProducers - 1) + 4 * (EG - 1));
+  static constexpr int kThreads = 32 * (kExtraWarp + (kProducers - 1) + 4 * (EG - 1) + 4);
   static constexpr int kEpi1Warp = kExtraWarp + kProducers - 1;  // first warp of epilogue group 1
+  static constexpr int kStage1Warp = kEpi1Warp + 4 * (EG - 1);   // first warp of the second staging set
   static constexpr int kXStageBytes = (kPairBN / 2) * (kBK / 2);  // this CTA's half of the routed rows
   static constexpr int kSfxStageBytes = 2 * kSfStageBytes;        // scales of up to two 128-row blocks
   static constexpr int kAccBufs = 2;
@@ -1001,12 +1002,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (even CTA, one thread) ----------------
-    // This one thread issues every MMA of the pair, and the tensor core finishes a
-    // stage's four MMAs in about the time a few dozen instructions take to issue
-    // here: the loop carries the stage's descriptor offsets and scale slot as
-    // running values (no multiplies or divisions), takes the wait's fast path
-    // inline, and issues the first K stage of a unit (which starts the
-    // accumulator) and a partial last stage outside the main loop.
+    // This one thread issues every MMA of the pair.  The tensor core queues only a
+    // stage's last MMA or two, so whatever this thread does between the last MMA of
+    // one stage and the first of the next leaves the tensor core idle: the next
+    // stage's bookkeeping and a non-blocking check of its scales-ready barrier are
+    // done between this stage's MMA issues (where the thread waits for queue room
+    // anyway), leaving only the commit and a fence in the gap.  Descriptors move as
+    // 32-bit low halves (the high halves are fixed for the kernel).
     if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -1014,12 +1016,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
       bool ok = true;
       const uint64_t adesc0 = smem_desc(smem_u32(s_w), 16, 1024, 2);
       const uint64_t bdesc0 = smem_desc(smem_u32(s_x), 16, 1024, 2);
+      const uint32_t a_lo0 = static_cast<uint32_t>(adesc0), a_hi = static_cast<uint32_t>(adesc0 >> 32);
+      const uint32_t b_lo0 = static_cast<uint32_t>(bdesc0), b_hi = static_cast<uint32_t>(bdesc0 >> 32);
       constexpr uint32_t kAStep = kWStageBytes >> 4, kBStep = C::kXStageBytes >> 4;  // descriptor units per stage
-      uint32_t ab_off = 0;  // stage * kAStep in the low half, stage * kBStep in the high half
+      uint32_t a_lo = a_lo0, b_lo = b_lo0;
       const uint32_t sf_base = tmem_base + C::kSfTmemBase;
-      uint32_t sf_col = sf_base;
+      const uint32_t sf_last = sf_base + (kPairSlots - 1) * kPairSlotCols;
+      uint32_t sfc = sf_base;
       const int KF = K / kBK;                      // full 256-element K stages
       const int k_tail = (K - KF * kBK) / 64;      // MMAs of a partial last stage (0-3)
+      const int n_st = KF + (k_tail > 0 ? 1 : 0);
       for (int u = pair; ok && u < total_units; u += npairs, ++acc_i) {
         const int b = acc_i % C::kAccBufs;
         if (!mbar_wait_bounded(&acc_empty[b], ((acc_i / C::kAccBufs) & 1) ^ 1u, p.timeout_ns, s_abort)) {
@@ -1027,40 +1033,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
           *s_abort = 1;
           break;
         }
-        tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kPairBN;
-        uint32_t idesc = 0;
-        for (int kt = 0; kt < KF + (k_tail > 0 ? 1 : 0); ++kt) {
-          // both CTAs staged this stage's scales: their copies of the stage have landed too
-          if (!mbar_try_wait(&sf_ready[stage], phase) &&
-              !mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
+        // first stage of the unit (starts the accumulator), and a unit of one partial stage
+        if (!mbar_spin_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 13);
+          *s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = idesc_mxf4nvf4(s_info[stage], 256);
+        int kt = 0;
+        bool next_ready = false;  // the next stage's scales-ready phase already seen complete
+        while (true) {
+          // stage kt's scales are ready (and fenced); issue its MMAs
+          const int n = kt < KF ? 4 : k_tail;
+          const uint32_t a_n = a_lo + kAStep, b_n = b_lo + kBStep;  // next stage's values, worked out in the
+          const int st_n = stage + 1 == S ? 0 : stage + 1;          // shadow of the MMA issues below
+          const uint32_t ph_n = stage + 1 == S ? phase ^ 1u : phase;
+          const uint32_t sfc_n = sfc == sf_last ? sf_base : sfc + kPairSlotCols;
+          const bool more = kt + 1 < n_st;
+          if (n == 4) {
+            mma_mxf4nvf4_pair_lo(d_tmem, a_lo, a_hi, b_lo, b_hi, idesc, sfc, sfc + 16, kt != 0 ? 1u : 0u);
+            mma_mxf4nvf4_pair_lo(d_tmem, a_lo + 2, a_hi, b_lo + 2, b_hi, idesc, sfc + 4, sfc + 22, 1u);
+            if (more) next_ready = mbar_test_wait(&sf_ready[st_n], ph_n);
+            mma_mxf4nvf4_pair_lo(d_tmem, a_lo + 4, a_hi, b_lo + 4, b_hi, idesc, sfc + 8, sfc + 28, 1u);
+            mma_mxf4nvf4_pair_lo(d_tmem, a_lo + 6, a_hi, b_lo + 6, b_hi, idesc, sfc + 12, sfc + 34, 1u);
+          } else {
+            for (int g = 0; g < n; ++g)
+              mma_mxf4nvf4_pair_lo(d_tmem, a_lo + 2 * g, a_hi, b_lo + 2 * g, b_hi, idesc, sfc + 4 * g,
+                                   sfc + 16 + 6 * g, (kt | g) != 0 ? 1u : 0u);
+            if (more) next_ready = mbar_test_wait(&sf_ready[st_n], ph_n);
+          }
+          mma_commit_pair(&empty[stage], 0x3);
+          stage = st_n;
+          phase = ph_n;
+          sfc = sfc_n;
+          a_lo = stage == 0 ? a_lo0 : a_n;
+          b_lo = stage == 0 ? b_lo0 : b_n;
+          if (!more) break;
+          ++kt;
+          if (!next_ready && !mbar_spin_bounded(&sf_ready[stage], phase, p.timeout_ns, s_abort)) {
             if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 13);
             *s_abort = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = adesc0 + (ab_off & 0xFFFFu);
-          const uint64_t bdesc = bdesc0 + (ab_off >> 16);
-          if (kt == 0) {
-            idesc = idesc_mxf4nvf4(s_info[stage], 256);
-            mma_mxf4nvf4_pair(d_tmem, adesc, bdesc, idesc, sf_col, sf_col + 16, 0u);
-            const int n = kt < KF ? 4 : k_tail;
-            for (int g = 1; g < n; ++g)
-              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g, 1u);
-          } else if (kt < KF) {
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g, 1u);
-          } else {
-            for (int g = 0; g < k_tail; ++g)
-              mma_mxf4nvf4_pair(d_tmem, adesc + 2 * g, bdesc + 2 * g, idesc, sf_col + 4 * g, sf_col + 16 + 6 * g, 1u);
-          }
-          mma_commit_pair(&empty[stage], 0x3);
-          sf_col += kPairSlotCols;
-          if (sf_col == sf_base + kPairSlots * kPairSlotCols) sf_col = sf_base;
-          ab_off += kAStep | (kBStep << 16);
-          if (++stage == S) { stage = 0; phase ^= 1u; ab_off = 0; }
         }
         if (!ok) break;
         mma_commit_pair(&acc_full[b], 0x3);
@@ -1069,8 +1087,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
       int zero = 0;
       mbar_wait_bounded(mma_done, 0, p.timeout_ns, reinterpret_cast<volatile int*>(&zero));
     }
-  } else if (warp >= 6 && warp < kExtraWarp) {
-    // ---------------- scale staging warps 6..9 (each CTA its own tensor memory) ----------------
+  } else if ((warp >= 6 && warp < kExtraWarp) || warp >= C::kStage1Warp) {
+    // ---------------- scale staging: two sets of four warps (6..9 and the last four) ----------------
+    // Each set takes every other fill: a staging warp's turn (wait, loads, tensor-memory
+    // stores, their completion, fence, arrive) takes longer than the tensor core needs for
+    // a stage, so two sets alternate.
     // Per fill, the 40 columns of the fill's slot in this warp's lane quadrant:
     // columns 4g..4g+3 the weight scales of K step g (only this quadrant's own
     // column is read by the MMA: weight row r's scales come from quadrant r/32),
@@ -1079,6 +1100,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
     const uint32_t quad_lane = (32u * quad) << 16;
     const uint32_t sf_ready_even = map_shared_rank(smem_u32(sf_ready), 0);
+    const int set = warp >= C::kStage1Warp ? 1 : 0;
+    const bool info_warp = warp == (set ? C::kStage1Warp : 6);  // quadrant 0 of the set: publishes unit info
     int stage = 0;
     uint32_t phase = 0;
     int fill = 0;
@@ -1097,11 +1120,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
       // column (o + c) % 4 of block (o + c) / 4, o = (x_row % 128) / 32
       const bool mid = (d.x_row & 127) != 0;
       for (int kt = 0; kt < KT; ++kt, ++fill) {
+        if ((fill & 1) != set) {  // the other set's fill
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+          continue;
+        }
         bool got = mbar_wait_bounded(&full[stage], phase, p.timeout_ns, s_abort);
-        if (got && fill >= kPairSlots) {
-          // the slot's previous fill (fill - kPairSlots) must be consumed by its MMAs
-          const int pf = fill - kPairSlots;
-          got = mbar_wait_bounded(&empty[pf % S], static_cast<uint32_t>(pf / S) & 1u, p.timeout_ns, s_abort);
+        // The scales go into registers before the wait for the slot, so only the stores
+        // and the hand-off follow the slot's release (the MMAs of fill - 3 completing).
+        uint32_t a[4], v[24];
+        if (__all_sync(0xffffffffu, got)) {
+          const uint8_t* sfw = s_w + stage * kWStageBytes + 16384 + lane * 16 + 4 * quad;
+          const uint8_t* sfx = s_sfx + stage * C::kSfxStageBytes + lane * 16;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            a[g] = *reinterpret_cast<const uint32_t*>(sfw + 512 * g);
+            const uint4 b0 = *reinterpret_cast<const uint4*>(sfx + 512 * g);
+            const uint4 b1 = *reinterpret_cast<const uint4*>(sfx + kSfStageBytes + 512 * g);
+            v[6 * g + 0] = mid ? b0.z : b0.x;
+            v[6 * g + 1] = mid ? b0.w : b0.y;
+            v[6 * g + 2] = mid ? b1.x : b0.z;
+            v[6 * g + 3] = mid ? b1.y : b0.w;
+            v[6 * g + 4] = mid ? b1.z : b1.x;
+            v[6 * g + 5] = mid ? b1.w : b1.y;
+          }
+          if (fill >= kPairSlots) {
+            // the slot's previous fill (fill - kPairSlots) must be consumed by its MMAs
+            const int pf = fill - kPairSlots;
+            got = mbar_wait_bounded(&empty[pf % S], static_cast<uint32_t>(pf / S) & 1u, p.timeout_ns, s_abort);
+          }
         }
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) {
@@ -1111,29 +1157,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
           ok = false;
           break;
         }
-        const uint8_t* sfw = s_w + stage * kWStageBytes + 16384 + lane * 16 + 4 * quad;
-        const uint8_t* sfx = s_sfx + stage * C::kSfxStageBytes + lane * 16;
-        uint32_t v[40];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t a = *reinterpret_cast<const uint32_t*>(sfw + 512 * g);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[4 * g + j] = (static_cast<uint32_t>(j) == quad) ? a : 0u;
-          const uint4 b0 = *reinterpret_cast<const uint4*>(sfx + 512 * g);
-          const uint4 b1 = *reinterpret_cast<const uint4*>(sfx + kSfStageBytes + 512 * g);
-          v[16 + 6 * g + 0] = mid ? b0.z : b0.x;
-          v[16 + 6 * g + 1] = mid ? b0.w : b0.y;
-          v[16 + 6 * g + 2] = mid ? b1.x : b0.z;
-          v[16 + 6 * g + 3] = mid ? b1.y : b0.w;
-          v[16 + 6 * g + 4] = mid ? b1.z : b1.x;
-          v[16 + 6 * g + 5] = mid ? b1.w : b1.y;
-        }
+        // weight scales: only this quadrant's own column of each K step (4g + quad) is read;
+        // routed-row scales: all 24 columns (every quadrant reads every routed row's scales)
         const uint32_t slot = tmem_base + quad_lane + C::kSfTmemBase + (fill % kPairSlots) * kPairSlotCols;
-        tmem_st_32cols(slot, *reinterpret_cast<const uint32_t(*)[32]>(v));
-        tmem_st_8cols(slot + 32, v + 32);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tmem_st_1col(slot + 4 * g + quad, a[g]);
+        tmem_st_16cols(slot + 16, v);
+        tmem_st_8cols(slot + 32, v + 16);
         tmem_st_wait();
         tc_fence_before();
-        if (kt == 0 && warp == 6 && lane == 0) s_info[stage] = d.n_mma;
+        if (kt == 0 && info_warp && lane == 0) s_info[stage] = d.n_mma;
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(sf_ready_even + stage * 8);
         if (++stage == S) { stage = 0; phase ^= 1u; }
