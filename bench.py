@@ -2,8 +2,10 @@
 
 One step = the whole layer over one batch: route + permute, quantise x into
 the routed rows, gate_up grouped GEMM with SiLU-mul + requantisation, down
-grouped GEMM with FINALIZE.  Default workload: the full decode layer with
-T=1024 tokens, E=256 experts, top-8, H=6144, I=2048 (uniform router logits).
+grouped GEMM with FINALIZE.  Default workload: the prefill layer with
+T=16384 tokens, E=256 experts, top-8, H=6144, I=2048 (uniform router logits),
+the largest of the layer configurations; the 1024-token decode layer on the
+same weights is measured in the same run (the line's decode_c4 entry).
 
 value: tokens/s of the layer with inputs resident in HBM (CUDA events on the
 launching stream over exactly --steps steps, after --warmup steps).  The
@@ -11,8 +13,12 @@ expert weights (5.4 GB of NVFP4) are far larger than L2 (129 MB), so every
 step streams them from HBM; no L2 flush is needed.
 e2e: the same through moe_forward with pinned host buffers: every step copies
 x and the logits to the device and the output back.
-roofline: the gate_up grouped GEMM (the largest kernel), algorithmic bytes per
-launch / its event-timed duration, against the measured HBM copy bandwidth.
+roofline: the gate_up grouped GEMM (the largest kernel).  At prefill it is
+bound by the tensor cores: its FLOPs over its event-timed duration against
+this GPU's dense NVFP4 MMA rate (the larger of the two probes, both in the
+line), with its HBM rate beside it.  At decode (decode_c4) it is bound by
+HBM: algorithmic bytes per launch over the duration against the measured
+copy bandwidth.
 cpu_baseline: the CPU oracle on a bounded sample of the same batch.
 
 --impl reference times the CPU oracle (the reference arm of this repo) on a
@@ -36,7 +42,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-T_DEF, E_DEF, K_DEF, H_DEF, I_DEF = 1024, 256, 8, 6144, 2048
+T_DEF, E_DEF, K_DEF, H_DEF, I_DEF = 16384, 256, 8, 6144, 2048
+DECODE_T_DEF = 1024
 METRIC = "MoE-layer tokens/s and grouped-GEMM TFLOPS & HBM GB/s vs roofline, 1 GB300"
 
 
@@ -52,6 +59,9 @@ def parse():
     ap.add_argument("--hidden", type=int, default=H_DEF)
     ap.add_argument("--intermediate", type=int, default=I_DEF)
     ap.add_argument("--zipf", type=float, default=None)
+    ap.add_argument("--decode-tokens", type=int, default=DECODE_T_DEF,
+                    help="also measure the layer at this many tokens on the same weights (the decode_c4 entry of "
+                         "the line; 0 to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="layer", choices=["layer", "gemm", "dense", "router"],
                     help="layer: the full MoE layer (default); gemm: one grouped GEMM, 256 experts x 32 rows, "
@@ -78,16 +88,18 @@ def kernel_source_digest() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the gate_up GEMM from the committed ncu record, or None when the record is
-    for another workload or for a kernel source that has changed since it was taken."""
+    """DRAM bytes per launch of the gate_up GEMM from the committed ncu records, or None when no record is
+    for this workload and the current kernel source (a record taken before the kernel changed is stale)."""
     try:
         with open(os.path.join(ROOT, "profiles", "gate_up_dram_traffic.json")) as f:
-            rec = json.load(f)
+            doc = json.load(f)
     except Exception:
         return None
-    if rec.get("workload") != workload or rec.get("kernel_sha256") != kernel_source_digest():
-        return None
-    return rec.get("dram_bytes_per_launch")
+    digest = kernel_source_digest()
+    for rec in doc.get("records", [doc]):
+        if rec.get("workload") == workload and rec.get("kernel_sha256") == digest:
+            return rec.get("dram_bytes_per_launch")
+    return None
 
 
 def peaks():
@@ -333,13 +345,30 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local_rank):
+def fp4_peaks(local_rank):
+    """This GPU's dense NVFP4 MMA rate from both probes (one CTA per SM with M = 128; CTA pairs with M = 256),
+    each timed over about half a second with the SM clock sampled meanwhile; the roofline takes the larger."""
+    import nvfp4_moe_grouped_gb300 as moe
+    out = {}
+    for name, pair in (("cta_m128", False), ("pair_m256", True)):
+        moe.fp4_mma_peak_tflops(iters=2000, reps=2, pair=pair)   # warm-up
+        with ClockSampler(local_rank) as clk:
+            clk.start()
+            rate = moe.fp4_mma_peak_tflops(iters=20000, reps=200, pair=pair)
+            clk.stop()
+        out[name] = {"tflops": rate, "clocks": clk.summary()}
+    out["peak_tflops"] = max(out["cta_m128"]["tflops"], out["pair_m256"]["tflops"])
+    return out
+
+
+def measure_layer(args, T, E, k, H, I, x, logits, pw13, pw2, dev, world, local_rank, e2e=True):
+    """One layer configuration through moe_forward: eager stage timing (each C-ABI stage bracketed by events on
+    the launching stream), the whole layer as one CUDA graph replayed back to back (the headline value, clocks
+    sampled meanwhile), and optionally the end-to-end run with pinned host buffers."""
+    import ctypes
+
     import nvfp4_moe_grouped_gb300 as moe
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    T, E, k, H, I = args.tokens, args.experts, args.top_k, args.hidden, args.intermediate
-    x, logits, pw13, pw2 = make_layer(T, E, k, H, I, args.zipf, dev)
     xd, ld = x.to(dev), logits.to(dev)
     fwd = moe.MoeForward(T, E, k, H, I, dev)
     h_scale = calibrate_h_scale(fwd, xd, ld, pw13)
@@ -347,76 +376,51 @@ def run_ours(args, rank, world, local_rank):
     P = L.padded_rows
     R = T * k
     stream = torch.cuda.current_stream()
-
-    # stage views inside the forward workspace (the same buffers moe_forward uses)
-    topk_id = fwd.view("topk_id", torch.int32, (T, k))
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-
-    def step(ev=None):
-        # the layer as its four C-ABI stages; events between them time each stage on this stream
-        r = route_into(fwd)
-        if ev is not None:
-            ev[0].record(stream)
-        quant_into(fwd, xd)
-        if ev is not None:
-            ev[1].record(stream)
-        gate_up_into(fwd, pw13, h_scale)
-        if ev is not None:
-            ev[2].record(stream)
-        down_into(fwd, pw2, out)
-        if ev is not None:
-            ev[3].record(stream)
-        return r
-
-    def route_into(f):
-        _call("moe_route_permute", f.lib.moe_route_permute(
-            _p(ld), T, E, k, f.ptr("topk_id"), f.ptr("topk_w"), f.ptr("expert_offsets"), f.ptr("perm_to_expanded"),
-            f.ptr("expanded_to_perm"), f.ptr("expanded_to_row"), f.ptr("route_ws"),
-            f.lib.moe_route_permute_workspace_size(T, E, k), _s()))
-
-    def quant_into(f, xdev):
-        _call("nvfp4_quantize", f.lib.nvfp4_quantize(
-            _p(xdev), 0, T, H, 1, f.ptr("x_scale"), 1, R, k, f.ptr("expanded_to_row"), f.ptr("x_codes"),
-            f.ptr("x_sf"), 1, P, f.ptr("quant_ws"), f.lib.nvfp4_quantize_workspace_size(1), _s()))
-
-    def gate_up_into(f, w, hs):
-        ep = moe.EpilogueArgs()
-        ep.h_scale = hs
-        ep.h_scale_out = f.ptr("h_scale")
-        ep.h_codes = f.ptr("h_codes")
-        ep.h_sf = f.ptr("h_sf")
-        _call("moe_grouped_gemm_nvfp4", f.lib.moe_grouped_gemm_nvfp4(
-            f.ptr("x_codes"), f.ptr("x_sf"), f.ptr("x_scale"), _p(w.blocked), _p(w.scale),
-            f.ptr("expert_offsets"), E, P, 2 * I, H, moe.EPI_SILU_MUL_QUANT, _byref(ep), None, None, 0, _s()))
-
-    def down_into(f, w, o):
-        ep = moe.EpilogueArgs()
-        ep.perm_to_expanded = f.ptr("perm_to_expanded")
-        ep.topk_w = f.ptr("topk_w")
-        ep.T = T
-        ep.k = k
-        wsb = f.lib.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, T, k, H)
-        _call("moe_grouped_gemm_nvfp4", f.lib.moe_grouped_gemm_nvfp4(
-            f.ptr("h_codes"), f.ptr("h_sf"), f.ptr("h_scale"), _p(w.blocked), _p(w.scale),
-            f.ptr("expert_offsets"), E, P, H, I, moe.EPI_FINALIZE, _byref(ep), _p(o), f.ptr("gemm_ws"), wsb, _s()))
-
-    import ctypes
-
-    def _p(t):
-        return ctypes.c_void_p(t.data_ptr())
-
-    def _s():
-        return ctypes.c_void_p(stream.cuda_stream)
-
-    def _byref(s):
-        return ctypes.byref(s)
+    lib = moe._lib.load()
+    ptr = lambda name: ctypes.c_void_p(fwd.ws.data_ptr() + getattr(L, name))
+    _p = lambda t: ctypes.c_void_p(t.data_ptr())
+    _s = lambda: ctypes.c_void_p(stream.cuda_stream)
 
     def _call(name, st):
         if st != 0:
             raise moe.MoeError(name, st)
 
-    fwd.lib = moe._lib.load()
-    fwd.ptr = lambda name: ctypes.c_void_p(fwd.ws.data_ptr() + getattr(L, name))
+    def step(ev=None):
+        # the layer as its four C-ABI stages; events between them time each stage on this stream
+        _call("moe_route_permute", lib.moe_route_permute(
+            _p(ld), T, E, k, ptr("topk_id"), ptr("topk_w"), ptr("expert_offsets"), ptr("perm_to_expanded"),
+            ptr("expanded_to_perm"), ptr("expanded_to_row"), ptr("route_ws"),
+            lib.moe_route_permute_workspace_size(T, E, k), _s()))
+        if ev is not None:
+            ev[0].record(stream)
+        _call("nvfp4_quantize", lib.nvfp4_quantize(
+            _p(xd), 0, T, H, 1, ptr("x_scale"), 1, R, k, ptr("expanded_to_row"), ptr("x_codes"),
+            ptr("x_sf"), 1, P, ptr("quant_ws"), lib.nvfp4_quantize_workspace_size(1), _s()))
+        if ev is not None:
+            ev[1].record(stream)
+        ep = moe.EpilogueArgs()
+        ep.h_scale = h_scale
+        ep.h_scale_out = ptr("h_scale")
+        ep.h_codes = ptr("h_codes")
+        ep.h_sf = ptr("h_sf")
+        _call("moe_grouped_gemm_nvfp4", lib.moe_grouped_gemm_nvfp4(
+            ptr("x_codes"), ptr("x_sf"), ptr("x_scale"), _p(pw13.blocked), _p(pw13.scale),
+            ptr("expert_offsets"), E, P, 2 * I, H, moe.EPI_SILU_MUL_QUANT, ctypes.byref(ep), None, None, 0, _s()))
+        if ev is not None:
+            ev[2].record(stream)
+        ep = moe.EpilogueArgs()
+        ep.perm_to_expanded = ptr("perm_to_expanded")
+        ep.topk_w = ptr("topk_w")
+        ep.T = T
+        ep.k = k
+        wsb = lib.moe_grouped_gemm_workspace_size(moe.EPI_FINALIZE, T, k, H)
+        _call("moe_grouped_gemm_nvfp4", lib.moe_grouped_gemm_nvfp4(
+            ptr("h_codes"), ptr("h_sf"), ptr("h_scale"), _p(pw2.blocked), _p(pw2.scale),
+            ptr("expert_offsets"), E, P, H, I, moe.EPI_FINALIZE, ctypes.byref(ep), _p(out), ptr("gemm_ws"), wsb,
+            _s()))
+        if ev is not None:
+            ev[3].record(stream)
 
     if args.profile_steps:
         for _ in range(max(1, args.warmup)):
@@ -427,7 +431,7 @@ def run_ours(args, rank, world, local_rank):
             step()
         torch.cuda.synchronize()
         torch.cuda.cudart().cudaProfilerStop()
-        return
+        return None
 
     for _ in range(args.warmup):
         step()
@@ -435,7 +439,7 @@ def run_ours(args, rank, world, local_rank):
     counts = np.diff(fwd.view("expert_offsets", torch.int32, (E + 1,)).cpu().numpy())
     ab = algorithmic_bytes(counts, T, E, k, H, I)
 
-    # ---- device-timed region
+    # ---- eager stage calls: per-stage launch times
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
@@ -447,8 +451,6 @@ def run_ours(args, rank, world, local_rank):
         step(evs[i])
     stop.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     eager_ms = start.elapsed_time(stop)
     prev = [start] + [evs[i][3] for i in range(args.steps - 1)]
     stage_ms = np.zeros(4)
@@ -469,8 +471,6 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
     weight_bytes = E * (2 * I * H + H * I) * 9 // 16
     flush = weight_bytes < (256 << 20)
     torch.cuda.synchronize()
@@ -491,6 +491,8 @@ def run_ours(args, rank, world, local_rank):
             clk.stop()
             ms = sum(a_.elapsed_time(b_) for a_, b_ in ev)
         else:
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
             g0.record(stream)
             for _ in range(args.steps):
                 graph.launch()
@@ -505,7 +507,11 @@ def run_ours(args, rank, world, local_rank):
     graph_last_stages = graph_st.stage_ms()
     ms = max_over_ranks(ms, dev)
     ms_step = ms / args.steps
-    value = whole_job_rate(T, world, ms_step)
+    res = {"T": T, "ms_step": ms_step, "value": whole_job_rate(T, world, ms_step), "stage_ms": stage_ms,
+           "graph_last_stages": graph_last_stages, "eager_ms": eager_ms / args.steps, "ab": ab, "h_scale": h_scale,
+           "clocks": clk.summary(), "flush": flush, "weight_bytes": weight_bytes}
+    if not e2e:
+        return res
 
     # ---- end to end through moe_forward with pinned host buffers
     # Every step copies its inputs from pinned host memory and reads its output back.  The copies of one
@@ -559,14 +565,65 @@ def run_ours(args, rank, world, local_rank):
     stream.wait_event(ev_in[(args.steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, dev)
-    e2e_value = whole_job_rate(T * args.steps, world, e2e_ms)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     # the output read back is the layer's output for these inputs (the device-timed graph computed it too;
     # FINALIZE's atomics may order the FP32 sums differently, so compare by relative difference)
     ref_out = out_g.float().cpu()
     e2e_rel = float((ohs[(args.steps - 1) & 1].float() - ref_out).norm() / max(float(ref_out.norm()), 1e-30))
+    res["e2e"] = {"value": whole_job_rate(T * args.steps, world, e2e_ms), "unit": "tokens/s",
+                  "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2,
+                  "how": "pinned H2D of x and logits, the layer graph, D2H of the output, every step; one step's "
+                         "copies overlap the previous step's layer (separate copy streams, two buffer sets)",
+                  "output_rel_diff_vs_device_run": e2e_rel}
+    return res
 
+
+def layer_roofline(r, k, H, I, fp4, hbm_peak, peak_kind, workload):
+    """Roofline of the gate_up GEMM launch of a measured layer: tensor-bound (its FLOPs against the larger
+    measured FP4 MMA rate, its HBM rate beside it) where experts see more than 48 routed rows on average,
+    HBM-bound (algorithmic bytes against the measured copy bandwidth) otherwise."""
+    T = r["T"]
+    ab = r["ab"]
+    ms = r["stage_ms"][2]
+    flops = 2.0 * T * k * 2 * I * H
+    hbm = ab["gate_up"] / (ms / 1e3) / 1e9
+    if T * k / max(1, ab["active_experts"]) > 48:
+        achieved = flops / (ms / 1e3) / 1e12
+        return {"bound": "tensor", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)",
+                "achieved": achieved, "peak": fp4["peak_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / fp4["peak_tflops"],
+                "peak_kind": "measured: the larger of this GPU's two dense NVFP4 MMA rate probes "
+                             "(moe_fp4_mma_probe, moe_fp4_mma_probe_pair)",
+                "traffic": recorded_traffic(workload), "algorithmic_flops_per_launch": flops, "launch_ms": ms,
+                "hbm_gbs": hbm, "hbm_frac": hbm / hbm_peak, "algorithmic_bytes_per_launch": ab["gate_up"]}
+    return {"bound": "hbm", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)", "achieved": hbm,
+            "peak": hbm_peak, "unit": "GB/s", "frac": hbm / hbm_peak, "peak_kind": peak_kind,
+            "traffic": recorded_traffic(workload), "algorithmic_bytes_per_launch": ab["gate_up"], "launch_ms": ms,
+            "tflops": flops / (ms / 1e3) / 1e12}
+
+
+def layer_workload_name(T, E, k, H, I, zipf):
+    return f"moe_layer_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{zipf}" if zipf else "_uniform")
+
+
+def run_ours(args, rank, world, local_rank):
+    import nvfp4_moe_grouped_gb300 as moe
+    from nvfp4_moe_grouped_gb300 import inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    T, E, k, H, I = args.tokens, args.experts, args.top_k, args.hidden, args.intermediate
+    x, logits, pw13, pw2 = make_layer(T, E, k, H, I, args.zipf, dev)
+    main_r = measure_layer(args, T, E, k, H, I, x, logits, pw13, pw2, dev, world, local_rank, e2e=True)
+    if main_r is None:   # --profile-steps: only the profiled steps ran
+        return
+    # the 1024-token decode layer on the same weights, measured in the same run
+    dec = None
+    Td = args.decode_tokens
+    if Td and Td != T:
+        xd4 = inputs.activations(Td, H)
+        ld4 = inputs.router_logits(Td, E, zipf_s=args.zipf)
+        dec = measure_layer(args, Td, E, k, H, I, xd4, ld4, pw13, pw2, dev, world, local_rank, e2e=False)
     code, where = moe.device_error()
     if code != 0:
         raise RuntimeError(f"device error {code} at {where} during the benchmark")
@@ -574,70 +631,67 @@ def run_ours(args, rank, world, local_rank):
         return
 
     hbm_peak, bf16_peak, peak_kind = peaks()
-    workload = f"moe_layer_T{T}_E{E}_k{k}_H{H}_I{I}" + (f"_zipf{args.zipf}" if args.zipf else "_uniform")
-    gate_up_ms = stage_ms[2]
-    flops_gate_up = 2.0 * T * k * 2 * I * H
-    fp4_peak = moe.fp4_mma_peak_tflops()
-    prefill = T * k / max(1, ab["active_experts"]) > 48
-    if prefill:
-        # compute-bound regime: FLOPs of the gate_up GEMM against the measured dense FP4 MMA rate
-        achieved = flops_gate_up / (gate_up_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)",
-                "achieved": achieved, "peak": fp4_peak, "unit": "TFLOP/s", "frac": achieved / fp4_peak,
-                "peak_kind": "measured (this GPU's dense NVFP4 MMA rate, moe_fp4_mma_probe)",
-                "traffic": None, "algorithmic_flops_per_launch": flops_gate_up, "launch_ms": gate_up_ms,
-                "hbm_gbs": ab["gate_up"] / (gate_up_ms / 1e3) / 1e9}
-    else:
-        achieved = ab["gate_up"] / (gate_up_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)",
-                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "peak_kind": peak_kind, "traffic": recorded_traffic(workload),
-                "algorithmic_bytes_per_launch": ab["gate_up"], "launch_ms": gate_up_ms}
+    fp4 = fp4_peaks(local_rank)
+    workload = layer_workload_name(T, E, k, H, I, args.zipf)
+    roof = layer_roofline(main_r, k, H, I, fp4, hbm_peak, peak_kind, workload)
+    stage_ms = main_r["stage_ms"]
+    gl = main_r["graph_last_stages"]
+    ms_step = main_r["ms_step"]
     flops_layer = 2.0 * T * k * (2 * I * H + H * I)
     cpu = None
     if not args.no_cpu_baseline:
         # a 2-token probe sizes the sample to about 12 s of oracle work (at most 64 tokens); preparing the
         # oracle's copy of each touched expert's weights is model setup and untimed
         cache = {}
-        dt2, _ = oracle_sample(x, logits, T, E, k, H, I, 2, h_scale, dev, cache)
+        dt2, _ = oracle_sample(x, logits, T, E, k, H, I, 2, main_r["h_scale"], dev, cache)
         n_tok = int(min(T, 64, max(2, math.ceil(12.0 / max(dt2 / 2, 1e-6)))))
-        dt, _ = oracle_sample(x, logits, T, E, k, H, I, n_tok, h_scale, dev, cache)
+        dt, _ = oracle_sample(x, logits, T, E, k, H, I, n_tok, main_r["h_scale"], dev, cache)
         cpu = {"value": n_tok / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"the first {n_tok} tokens of the batch (their {n_tok * k} expert rows), one pass, "
                          f"{dt:.1f} s of oracle work"}
+    decode_line = None
+    if dec is not None:
+        dw = layer_workload_name(Td, E, k, H, I, args.zipf)
+        decode_line = {
+            "workload": dw, "value": dec["value"], "unit": "tokens/s", "ms_per_step": dec["ms_step"],
+            "roofline": layer_roofline(dec, k, H, I, fp4, hbm_peak, peak_kind, dw),
+            "stages_ms": {"route_permute": dec["stage_ms"][0], "quantize_x": dec["stage_ms"][1],
+                          "gate_up_gemm": dec["stage_ms"][2], "down_gemm_finalize": dec["stage_ms"][3],
+                          "source": f"eager stage calls, mean of {args.steps} steps"},
+            "hbm_gbs_layer": dec["ab"]["layer"] / (dec["ms_step"] / 1e3) / 1e9,
+            "clocks": dec["clocks"]}
+    weight_bytes = main_r["weight_bytes"]
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": main_r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e2m1xe2m1->f32", "data": "synthetic",
         "config": {"workload": workload,
                    "tokens": T, "experts": E, "top_k": k, "hidden": H, "intermediate": I,
                    "l2": (f"weights ({weight_bytes / 1e9:.3f} GB) below 256 MB: L2 flushed (256 MB write) "
-                          f"before each timed step" if flush else
+                          f"before each timed step" if main_r["flush"] else
                           f"weights ({weight_bytes / 1e9:.2f} GB) exceed L2 (129 MB); no flush"),
                    "parallelism": f"replicas{world}"},
         "roofline": roof,
-        "fp4_mma_probe_tflops": fp4_peak,
+        "fp4_mma_probe_tflops": fp4["peak_tflops"],
+        "fp4_mma_probes": fp4,
         "stages_ms": {"route_permute": stage_ms[0], "quantize_x": stage_ms[1], "gate_up_gemm": stage_ms[2],
                       "down_gemm_finalize": stage_ms[3], "source": f"eager stage calls, mean of {args.steps} steps"},
-        "graph_last_step_stages_ms": {"route_permute": graph_last_stages[0], "quantize_x": graph_last_stages[1],
-                                      "gate_up_gemm": graph_last_stages[2],
-                                      "down_gemm_finalize": graph_last_stages[3], "layer": graph_last_stages[4]},
-        "eager_ms_per_step": eager_ms / args.steps,
-        "timing": "value: CUDA-graph replays of the whole layer (moe_forward_graph_launch, no stage-timing nodes) back to back; "
-                  "roofline.launch_ms: the gate_up GEMM launch inside eager stage calls timed with events "
-                  "on the launching stream",
-        "gemm_tflops": {"gate_up": flops_gate_up / (gate_up_ms / 1e3) / 1e12,
+        "graph_last_step_stages_ms": {"route_permute": gl[0], "quantize_x": gl[1], "gate_up_gemm": gl[2],
+                                      "down_gemm_finalize": gl[3], "layer": gl[4]},
+        "eager_ms_per_step": main_r["eager_ms"],
+        "timing": "value: CUDA-graph replays of the whole layer (moe_forward_graph_launch, no stage-timing nodes) "
+                  "back to back; roofline.launch_ms: the gate_up GEMM launch inside eager stage calls timed with "
+                  "events on the launching stream",
+        "gemm_tflops": {"gate_up": 2.0 * T * k * 2 * I * H / (stage_ms[2] / 1e3) / 1e12,
                         "down": 2.0 * T * k * H * I / (stage_ms[3] / 1e3) / 1e12,
                         "layer": flops_layer / (ms_step / 1e3) / 1e12},
-        "hbm_gbs_layer": ab["layer"] / (ms_step / 1e3) / 1e9,
-        "active_experts": ab["active_experts"],
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
-                "d2h_bytes_per_step": T * H * 2,
-                "how": "pinned H2D of x and logits, the layer graph, D2H of the output, every step; one step's "
-                       "copies overlap the previous step's layer (separate copy streams, two buffer sets)",
-                "output_rel_diff_vs_device_run": e2e_rel},
+        "hbm_gbs_layer": main_r["ab"]["layer"] / (ms_step / 1e3) / 1e9,
+        "active_experts": main_r["ab"]["active_experts"],
+        "e2e": main_r["e2e"],
+        "decode_c4": decode_line,
+        # per step: routing 3, amax + quantiser 2, gate_up GEMM, down GEMM, FP32 -> BF16
         "gpu_launches": 8 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": main_r["clocks"],
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
