@@ -76,14 +76,39 @@ def parse():
     return ap.parse_args()
 
 
+def _code_only(src: str) -> str:
+    """C/C++ source with its comments removed and whitespace runs collapsed (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest() -> str:
-    """SHA-256 of the grouped-GEMM source and the headers it includes (identifies the measured kernel)."""
+    """SHA-256 of the code (comments and layout stripped) of the grouped-GEMM source and the headers it
+    includes: identifies the measured kernel."""
     import hashlib
     h = hashlib.sha256()
     for rel in ("nvfp4_moe_grouped_gb300/csrc/grouped_gemm.cu", "nvfp4_moe_grouped_gb300/csrc/common.cuh",
                 "include/nvfp4_moe.h"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

@@ -740,8 +740,9 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
 // next one is refilled.
 // Roles per CTA: warps 0 and 10-11 (10-12) issue copies (each CTA its own halves),
 // warp 1 owns tensor memory (in the even CTA its lane 0 issues the MMAs),
-// warps 6-9 stage scales into their own CTA's tensor memory and tell the even
-// CTA, warps 2-5 (and 12-15) drain the accumulator and run the epilogue.
+// two sets of four warps (6-9 and the CTA's last four) take alternate stage
+// fills, stage their scales into their own CTA's tensor memory and tell the
+// even CTA, warps 2-5 (and 12-15) drain the accumulator and run the epilogue.
 // Signals between the CTAs: the MMA thread's commits arrive on both CTAs'
 // stage-empty and accumulator-full barriers (one multicast commit each); the
 // staging and epilogue warps of both CTAs arrive on the even CTA's
@@ -755,7 +756,7 @@ constexpr int kPairSlots = 3;              // tensor-memory scale slots
 constexpr uint32_t kPairSlotCols = 40;     // 16 weight-scale + 24 routed-row-scale columns
 
 // EG = epilogue warp groups.  With two groups, three copy warps (0, 10, 11) keep
-// the CTA at 16 warps (128 registers each); with one, four (0, 10-12).
+// the CTA at 20 warps; with one, four copy warps (0, 10-12) make 17.
 template <int EG>
 struct PairCfg {
   static constexpr int kProducers = EG == 2 ? 3 : 4;
