@@ -370,6 +370,10 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+FP4_PEAK_KIND = ("measured: the larger of this GPU's two dense NVFP4 MMA rate probes (moe_fp4_mma_probe, "
+                 "moe_fp4_mma_probe_pair)")
+
+
 def fp4_peaks(local_rank):
     """This GPU's dense NVFP4 MMA rate from both probes (one CTA per SM with M = 128; CTA pairs with M = 256),
     each timed over about half a second with the SM clock sampled meanwhile; the roofline takes the larger."""
@@ -617,8 +621,7 @@ def layer_roofline(r, k, H, I, fp4, hbm_peak, peak_kind, workload):
         return {"bound": "tensor", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)",
                 "achieved": achieved, "peak": fp4["peak_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / fp4["peak_tflops"],
-                "peak_kind": "measured: the larger of this GPU's two dense NVFP4 MMA rate probes "
-                             "(moe_fp4_mma_probe, moe_fp4_mma_probe_pair)",
+                "peak_kind": FP4_PEAK_KIND,
                 "traffic": recorded_traffic(workload), "algorithmic_flops_per_launch": flops, "launch_ms": ms,
                 "hbm_gbs": hbm, "hbm_frac": hbm / hbm_peak, "algorithmic_bytes_per_launch": ab["gate_up"]}
     return {"bound": "hbm", "kernel": "grouped_gemm gate_up (SiLU-mul + requant epilogue)", "achieved": hbm,
@@ -838,8 +841,9 @@ def run_dense(args, rank, world, local_rank):
     ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     flops = 2.0 * M * N * K
     tf = flops / (ms / 1e3) / 1e12
-    peak_fp4 = moe.fp4_mma_peak_tflops()
+    fp4 = fp4_peaks(local_rank) if rank == 0 else None
     if rank == 0:
+        peak_fp4 = fp4["peak_tflops"]
         print(json.dumps({
             "metric": "dense NVFP4 GEMM TFLOPS vs dense FP4 peak", "value": tf, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -850,8 +854,9 @@ def run_dense(args, rank, world, local_rank):
                               else f"inputs ({in_bytes / 2**20:.0f} MB) exceed L2; no flush")},
             "roofline": {"bound": "tensor", "kernel": "grouped_gemm NONE (one group)", "achieved": tf,
                          "peak": peak_fp4, "unit": "TFLOP/s", "frac": tf / peak_fp4,
-                         "peak_kind": "measured (this GPU's dense NVFP4 MMA rate, moe_fp4_mma_probe)",
+                         "peak_kind": FP4_PEAK_KIND,
                          "traffic": None, "algorithmic_flops_per_launch": flops, "launch_ms": ms},
+            "fp4_mma_probes": fp4,
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 
@@ -911,12 +916,12 @@ def run_gated(args, rank, world, local_rank):
     if T * k / max(1, ab["active_experts"]) > 48:
         # compute-bound regime (as for the layer workload): the whole graph's expert-GEMM FLOPs against the
         # measured dense FP4 MMA rate
-        fp4_peak = moe.fp4_mma_peak_tflops()
+        fp4_peak = fp4_peaks(local_rank)["peak_tflops"]
         flops = 2.0 * T * k * (2 * I * H + H * I)
         tf = flops / (ms / 1e3) / 1e12
         roof = {"bound": "tensor", "kernel": "whole layer with the router (one CUDA graph)", "achieved": tf,
                 "peak": fp4_peak, "unit": "TFLOP/s", "frac": tf / fp4_peak,
-                "peak_kind": "measured (this GPU's dense NVFP4 MMA rate, moe_fp4_mma_probe)", "traffic": None,
+                "peak_kind": FP4_PEAK_KIND, "traffic": None,
                 "algorithmic_flops_per_launch": flops, "launch_ms": ms, "hbm_gbs": gbs}
     else:
         roof = {"bound": "hbm", "kernel": "whole layer with the router (one CUDA graph)", "achieved": gbs,
