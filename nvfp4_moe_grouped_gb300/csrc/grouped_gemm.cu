@@ -159,7 +159,7 @@ struct GemmParams {
 };
 
 struct Unit {
-  int e, nb, mt, rows, n_mma, x_row, m_off;
+  int e, nb, nbe, mt, rows, n_mma, x_row, m_off;
   bool valid;  // false when the offsets place the unit outside the operands (the launch then stops)
 };
 
@@ -182,9 +182,13 @@ MOE_DEVINL int find_expert_from(const int* start, int E, int u, int e) {
   return lo;
 }
 
-// Unit u -> (column chunk c, expert e, routed-row block nb, weight tile mt):
-// U units per chunk, ordered expert-major, each routed-row block taking MTC
-// consecutive units (the chunk's weight tiles).
+// Unit u -> (column chunk c, expert e, weight tile mt, routed-row block nb):
+// U units per chunk, ordered expert-major; inside an expert, weight tile by
+// weight tile, with the expert's nbe routed-row blocks of one weight tile on
+// consecutive units.  Consecutive units run on different CTAs at about the same
+// time, so when a busy expert has several routed-row blocks, the CTAs reading
+// one weight tile for its different blocks run together and share it in L2
+// (the first read brings it from HBM).
 template <int BN>
 MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, const int* off, int E, int MTC, int U,
                             int64_t rows_alloc, int64_t items, int& e_hint) {
@@ -194,8 +198,10 @@ MOE_DEVINL Unit decode_unit(int u, const int* unit_start, const int* pad_start, 
   if (unit_start[e_hint] > uc) e_hint = 0;  // a new column chunk starts over at expert 0
   d.e = e_hint = find_expert_from(unit_start, E, uc, e_hint);
   const int local = uc - unit_start[d.e];
-  d.nb = local / MTC;
-  d.mt = c * MTC + (local - d.nb * MTC);
+  d.nbe = (unit_start[d.e + 1] - unit_start[d.e]) / MTC;
+  const int mtl = local / d.nbe;
+  d.nb = local - mtl * d.nbe;
+  d.mt = c * MTC + mtl;
   const int m_e = off[d.e + 1] - off[d.e];
   d.rows = min(BN, m_e - d.nb * BN);
   d.n_mma = d.rows <= 32 ? 32 : (d.rows <= 64 ? 64 : 128);
@@ -439,7 +445,10 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
     const int pid = warp == 0 ? 0 : warp - kExtraWarp + 1;
     int* s_last = reinterpret_cast<int*>(smem + C::last);  // [kProducers][S] last fill index per stage
     if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
+      // a weight tile with one reader (an expert with one routed-row block) at
+      // evict-first; one that the expert's other blocks read at the same time
+      // at normal priority, so those reads hit L2
+      const uint64_t pol_w1 = l2_policy_evict_first(), pol_wn = l2_policy_evict_normal();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -457,6 +466,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
         }
         const uint8_t* w_src = p.w_blocked + static_cast<int64_t>(d.e * MT + d.mt) * KT * kWStageBytes;
         const uint8_t* sfx_src = p.x_sf + static_cast<int64_t>(d.x_row / 128) * (K / 64) * 512;
+        const uint64_t pol_w = d.nbe > 1 ? pol_wn : pol_w1;
         for (int kt = 0; kt < KT; ++kt, ++fill) {
           if (fill % kProducers == pid) {
             if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, s_abort)) {
@@ -795,7 +805,7 @@ struct PairUnit {
   bool valid;
 };
 
-// Pair unit u -> (column chunk, expert e, 192-row block nb, weight tile pair mt2);
+// Pair unit u -> (column chunk, expert e, weight tile pair mt2, 192-row block nb);
 // the same order as decode_unit with MTC weight tile pairs per chunk.
 MOE_DEVINL PairUnit decode_pair_unit(int u, const int* unit_start, const int* pad_start, const int32_t* off, int E,
                                      int MTC, int U, int64_t rows_alloc, int64_t items, int& e_hint) {
@@ -805,8 +815,10 @@ MOE_DEVINL PairUnit decode_pair_unit(int u, const int* unit_start, const int* pa
   if (unit_start[e_hint] > uc) e_hint = 0;
   d.e = e_hint = find_expert_from(unit_start, E, uc, e_hint);
   const int local = uc - unit_start[d.e];
-  d.nb = local / MTC;
-  d.mt2 = c * MTC + (local - d.nb * MTC);
+  const int nbe = (unit_start[d.e + 1] - unit_start[d.e]) / MTC;
+  const int mtl = local / nbe;
+  d.nb = local - mtl * nbe;
+  d.mt2 = c * MTC + mtl;
   const int o0 = __ldg(off + d.e);  // expert offsets straight from global memory (L1-cached)
   const int m_e = __ldg(off + d.e + 1) - o0;
   d.rows = min(kPairBN, m_e - d.nb * kPairBN);
@@ -943,10 +955,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
     const int pid = warp == 0 ? 0 : warp - kExtraWarp + 1;
     int* s_last = reinterpret_cast<int*>(smem + C::last);
     if (lane == 0) {
-      // Each weight tile pair is read by the pairs working on the expert's other routed-row
-      // blocks at about the same time, so weights stay in L2 at normal priority here (evict-first
-      // suits the decode kernel, where a weight tile has one reader); routed rows, read once
-      // per weight tile pair, at evict-last.
       // Each weight tile pair is read by the pairs working on the expert's other routed-row
       // blocks at about the same time, so weights stay in L2 at normal priority (measured:
       // gate_up 1.66 -> 1.63 ms at 16384 tokens), except under FINALIZE, whose FP32 atomics need
