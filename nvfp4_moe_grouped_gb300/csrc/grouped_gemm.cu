@@ -662,9 +662,29 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
       }
       if (acc_i % C::kEpiGroups != eg) continue;  // the other group drains this unit
       const int b = acc_i % C::kAccBufs;
+      const float alpha = x_scale * __ldg(p.w_scale + d.e);
+      int* tok_tab = s_tok_t + (acc_i & 1) * BN;
+      float* w_tab = s_tok_w + (acc_i & 1) * BN;
+      if (p.epilogue == MOE_EPI_FINALIZE) {
+        // Token table of this unit: routed row et -> destination row (token, or
+        // expanded item when gathering) and router weight x alpha, built before the
+        // accumulator wait so that its dependent global loads overlap the mainloop.
+        // With one group it is double-buffered (the barrier after the previous
+        // unit's table orders the reads of this buffer two units back before this
+        // write); with two, each group's buffer is released by the barrier that
+        // ends the group's previous unit.
+        if (et < d.rows) {
+          const int ex = __ldg(p.perm_to_expanded + d.m_off + et);
+          const bool in_range = ex >= 0 && ex < p.T * p.k;
+          if (!in_range) record_error(p.err, MOE_ERR_INVALID_ARG, 6);
+          tok_tab[et] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
+          w_tab[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
+        }
+      }
       const bool got = mbar_wait_bounded(&acc_full[b], (acc_i / C::kAccBufs) & 1, p.timeout_ns, s_abort);
       // The four warps of the group decide together, so none is left waiting on a
-      // named barrier that the others have abandoned.
+      // named barrier that the others have abandoned; the barrier also publishes
+      // the token table to the group.
       if (epi_any(eg, !got)) {
         if (et == 0) {
           if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 4);
@@ -673,24 +693,7 @@ __global__ void __launch_bounds__(Cfg<BN, EG>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float alpha = x_scale * __ldg(p.w_scale + d.e);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * C::kAccCols;
-      int* tok_tab = s_tok_t + (acc_i & 1) * BN;
-      float* w_tab = s_tok_w + (acc_i & 1) * BN;
-      if (p.epilogue == MOE_EPI_FINALIZE) {
-        // Token table of this unit: routed row et -> destination row (token, or
-        // expanded item when gathering) and router weight x alpha.  Double-buffered:
-        // the barrier below also orders the reads of the other buffer two units
-        // back before this write.
-        if (et < d.rows) {
-          const int ex = __ldg(p.perm_to_expanded + d.m_off + et);
-          const bool in_range = ex >= 0 && ex < p.T * p.k;
-          if (!in_range) record_error(p.err, MOE_ERR_INVALID_ARG, 6);
-          tok_tab[et] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
-          w_tab[et] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
-        }
-        epi_bar(eg);
-      }
       const SiluOut so{p.h_scale, p.h_codes, p.h_sf, p.h_f32, N / 2};
       for (int j0 = 0; j0 < d.rows; j0 += 32) {
         uint32_t r[32];
@@ -1226,19 +1229,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
       }
       if (acc_i % EG != eg) continue;
       const int b = acc_i % C::kAccBufs;
-      const bool got = mbar_wait_bounded(&acc_full[b], (acc_i / C::kAccBufs) & 1, p.timeout_ns, s_abort);
-      if (epi_any(eg, !got)) {
-        if (et == 0) {
-          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 15);
-          *s_abort = 1;
-        }
-        break;
-      }
-      tc_fence_after();
       const int mt = 2 * d.mt2 + static_cast<int>(rank);
       const float alpha = x_scale * __ldg(p.w_scale + d.e);
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kPairBN;
       // token table double-buffered per group: this group's unit before last read the other half
+      // (the barrier after the previous unit's table orders those reads before this write).  It is
+      // built before the accumulator wait, so its dependent global loads overlap the mainloop.
       int* tok_tab = s_tok_t + (eg * 2 + ((acc_i / EG) & 1)) * kPairBN;
       float* w_tab = s_tok_w + (eg * 2 + ((acc_i / EG) & 1)) * kPairBN;
       if (p.epilogue == MOE_EPI_FINALIZE) {
@@ -1249,8 +1244,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EG>::kThread
           tok_tab[i] = in_range ? (p.fin_gather ? ex : ex / p.k) : -1;
           w_tab[i] = in_range ? __ldg(p.topk_w + ex) * alpha : 0.0f;
         }
-        epi_bar(eg);
       }
+      const bool got = mbar_wait_bounded(&acc_full[b], (acc_i / C::kAccBufs) & 1, p.timeout_ns, s_abort);
+      // the OR-reduction barrier also publishes the token table to the whole group
+      if (epi_any(eg, !got)) {
+        if (et == 0) {
+          if (!*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 15);
+          *s_abort = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + b * kPairBN;
       for (int j0 = 0; j0 < d.rows; j0 += 32) {
         uint32_t r[32];
         tmem_ld_32cols(taddr + j0, r);
