@@ -717,8 +717,9 @@ def run_ours(args, rank, world, local_rank):
         "active_experts": main_r["ab"]["active_experts"],
         "e2e": main_r["e2e"],
         "decode_c4": decode_line,
-        # per step: routing 3, amax + quantiser 2, gate_up GEMM, down GEMM, FP32 -> BF16
-        "gpu_launches": 8 * args.steps,
+        # per step: routing (1 or 3), amax + quantiser, gate_up GEMM, down GEMM, FP32 -> BF16; or the
+        # single-launch layer for small shapes
+        "gpu_launches": moe.forward_kernel_count(T, E, k, H, I) * args.steps,
         "clocks": main_r["clocks"],
         "cpu_baseline": cpu,
     }

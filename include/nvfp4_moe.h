@@ -98,7 +98,7 @@ enum { MOE_EPI_NONE = 0, MOE_EPI_SILU_MUL_QUANT = 1, MOE_EPI_FINALIZE = 2 };
 MOE_API const char* moe_status_string(int status);
 
 /* ABI version of this header; bumped on any incompatible change (3: FINALIZE workspace query takes k;
- * 4: moe_router takes x_scale; 5: moe_finalize takes y_rows). */
+ * 4: moe_router takes x_scale; 5: moe_finalize takes y_rows; 6: the forward layout has small_scratch). */
 MOE_API int moe_abi_version(void);
 
 /* Reads and clears the device error word written by bounded waits that gave
@@ -114,8 +114,9 @@ MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
 /* Test hooks: bit 0 makes the next grouped-GEMM launches skip filling their
  * first pipeline stage, so the bounded-wait path can be exercised without
  * faulting anything; bit 1 makes them keep the one-CTA 128-row tile where
- * the CTA-pair tile would run, so both kernels can be compared on one input.
- * 0 (the default) for normal operation. */
+ * the CTA-pair tile would run, so both kernels can be compared on one input;
+ * bit 2 makes moe_forward (and its graph) use the staged kernels for layers
+ * the single-launch path would take.  0 (the default) for normal operation. */
 MOE_API void moe_debug_set_flags(int flags);
 
 /* Bytes of a blocked weight buffer of `rows` rows (rows % 128 == 0) and K
@@ -391,9 +392,25 @@ typedef struct {
 typedef struct {
   size_t topk_id, topk_w, expert_offsets, perm_to_expanded, expanded_to_perm, expanded_to_row;
   size_t x_scale, x_codes, x_sf, h_scale, h_codes, h_sf, route_ws, quant_ws, gemm_ws;
+  size_t small_scratch; /* scratch of the single-launch path; (size_t)-1 for layers it does not take */
   int64_t padded_rows; /* rows allocated for the routed-row buffers */
   size_t total;
 } moe_forward_layout;
+
+/* Small layers (T * k <= 64, E <= 64, H <= 1024, I <= 512) run as ONE kernel
+ * ("Tracing the Failure ...", "Conclusion": persistent kernel designs against
+ * per-kernel overheads): one CTA per expert routes every token itself, takes
+ * x's amax itself, quantises its rows, runs both contractions on the CUDA cores
+ * and writes each routed row times its router weight to small_scratch; the last
+ * CTA to finish sums every token's k rows in slot order into `out`.  Every
+ * intermediate of the layout is written as the staged kernels write it: the
+ * routing and permutation and the quantised x are the same bits, and h and out
+ * differ only by the order of the FP32 sums in the contractions.  A ticket word
+ * at the end of small_scratch is left at 0 by every launch (moe_forward clears
+ * it first; a graph relies on the eager pass of its creation).
+ * moe_forward_kernel_count: kernels one moe_forward call (or one replay of its
+ * graph) launches for this shape, 0 for an invalid shape. */
+MOE_API int moe_forward_kernel_count(int T, int E, int k, int H, int I);
 
 MOE_API size_t moe_forward_workspace_size(int T, int E, int k, int H, int I);
 MOE_API moe_status moe_forward_workspace_layout(int T, int E, int k, int H, int I, moe_forward_layout* layout);

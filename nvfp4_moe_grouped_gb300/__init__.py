@@ -25,7 +25,7 @@ EPI_NONE, EPI_SILU_MUL_QUANT, EPI_FINALIZE = 0, 1, 2
 SF_LINEAR, SF_TILED, SF_BLOCKED = 0, 1, 2
 
 __all__ = ["moe_route_permute", "nvfp4_quantize", "moe_grouped_gemm_nvfp4", "moe_finalize", "moe_forward",
-           "prepare_expert_weights", "MoeForward", "padded_rows_max", "device_error", "EPI_NONE",
+           "prepare_expert_weights", "MoeForward", "padded_rows_max", "forward_kernel_count", "device_error", "EPI_NONE",
            "EPI_SILU_MUL_QUANT", "EPI_FINALIZE", "SF_LINEAR", "SF_TILED", "SF_BLOCKED", "MoeError",
            "EpilogueArgs", "ForwardGraph"]
 
@@ -60,6 +60,11 @@ def _empty(shape, dtype, device):
 
 def padded_rows_max(routed_rows: int, E: int) -> int:
     return int(_L().moe_padded_rows_max(routed_rows, E))
+
+
+def forward_kernel_count(T: int, E: int, k: int, H: int, I: int) -> int:
+    """Kernels one moe_forward call (or graph replay) launches for this layer shape."""
+    return int(_L().moe_forward_kernel_count(T, E, k, H, I))
 
 
 def device_error():

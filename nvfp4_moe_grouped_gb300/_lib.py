@@ -43,7 +43,8 @@ class ForwardLayout(ctypes.Structure):
     """Mirror of moe_forward_layout."""
     _fields_ = [(n, c_size_t) for n in (
         "topk_id", "topk_w", "expert_offsets", "perm_to_expanded", "expanded_to_perm", "expanded_to_row",
-        "x_scale", "x_codes", "x_sf", "h_scale", "h_codes", "h_sf", "route_ws", "quant_ws", "gemm_ws")] + [
+        "x_scale", "x_codes", "x_sf", "h_scale", "h_codes", "h_sf", "route_ws", "quant_ws", "gemm_ws",
+        "small_scratch")] + [
         ("padded_rows", c_int64), ("total", c_size_t)]
 
 
@@ -76,6 +77,7 @@ SIGNATURES = {
     "moe_forward_gated": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,
                                   c_void_p, c_size_t, c_void_p]),
     "moe_forward_workspace_layout": (c_int, [c_int] * 5 + [c_void_p]),
+    "moe_forward_kernel_count": (c_int, [c_int] * 5),
     "moe_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_void_p,
                             c_void_p, c_size_t, c_void_p]),
     "moe_forward_graph_create": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,

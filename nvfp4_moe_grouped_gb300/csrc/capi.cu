@@ -64,7 +64,7 @@ extern "C" const char* moe_status_string(int status) {
   }
 }
 
-extern "C" int moe_abi_version(void) { return 5; }
+extern "C" int moe_abi_version(void) { return 6; }
 
 extern "C" moe_status moe_device_error(int32_t* code, int32_t* where) {
   if (!code || !where) return MOE_ERR_INVALID_ARG;

@@ -94,6 +94,43 @@ MOE_DEVINL float route_exp(float x) {
   return __fmul_rn(p, two_n);
 }
 
+// Larger of two (value, index) routing candidates: higher value, then lower index.
+MOE_DEVINL bool route_better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+
+// Top-k and softmax of one token whose E logits a warp holds: lane l owns
+// experts l + 32 i in v[i], and bit i of `taken` is set where that expert does
+// not exist (>= E).  Slot j (descending logit, ties to the lower index) ends in
+// lane j: *id its expert, *w its weight, the softmax of the k selected logits
+// (exponentials of the differences to the largest, summed in slot order, one
+// correctly rounded division).  Lanes >= k get *w = 0 and an unspecified *id.
+template <int NV>
+MOE_DEVINL void warp_topk_softmax(const float (&v)[NV], uint32_t taken, int k, int* id, float* w) {
+  const int lane = threadIdx.x & 31;
+  float my_v = 0.0f;
+  int my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -__int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (!(taken >> i & 1u) && route_better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (route_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) { my_v = bv; my_i = bi; }
+  }
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = (lane < k) ? route_exp(__fsub_rn(my_v, m)) : 0.0f;
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+  *id = my_i;
+  *w = (lane < k) ? __fdiv_rn(ex, sum) : 0.0f;
+}
+
 // e2m1 codes of eight values, v[i] in bits 4i..4i+3: the nearest of
 // {0, .5, 1, 1.5, 2, 3, 4, 6} with the sign, ties to the even code, saturating
 // above 6 (the hardware conversion, two values per instruction, the first
@@ -145,6 +182,17 @@ MOE_DEVINL uint32_t nvfp4_codes8(const float* x, float recip) {
   for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(x[i], recip);
   return e2m1x8(v);
 }
+
+// h = silu(g) * u = g / (1 + e^-g) * u in FP32 with the fast hardware forms:
+// __expf (the SFU's 2^x, error growing with |g|) and __fdividef (about 2 ulp),
+// then a correctly rounded product.  Against the FP64 reference on the
+// full-size layers, these flip 16 of 524,288 sampled requantised h codes (one
+// grid step each, at rounding boundaries) in one of nine configurations and none
+// in the other eight; correctly rounded division and expf flip none there, but
+// cost the prefill gate_up launch about a quarter of its time (its epilogue
+// shares the SM with the MMA issue).  For g below about -88 the quotient is -0,
+// the limit of silu there.
+MOE_DEVINL float silu_mul(float g, float u) { return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u); }
 
 MOE_DEVINL float bf16_bits_to_float(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 

@@ -10,6 +10,15 @@
 
 namespace moe {
 int32_t* route_pad_offsets(void* ws, int T, int E, int k);
+int& gemm_debug_flags();
+bool small_layer_eligible(int T, int E, int k, int H, int I);
+size_t small_layer_scratch_bytes(int T, int k, int H);
+moe_status small_layer_enqueue(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k,
+                               int H, int I, float h_scale, uint16_t* out, int32_t* topk_id, float* topk_w,
+                               int32_t* offs, int32_t* p2e, int32_t* e2p, int32_t* e2r, float* x_scale,
+                               uint8_t* x_codes, uint8_t* x_sf, float* hs, uint8_t* h_codes, uint8_t* h_sf,
+                               void* scratch, bool clear_ticket, cudaStream_t st);
+bool route_one_chunk(int T, int E, int k);
 }
 
 using namespace moe;
@@ -39,9 +48,26 @@ extern "C" moe_status moe_forward_workspace_layout(int T, int E, int k, int H, i
   L->route_ws = take(moe_route_permute_workspace_size(T, E, k));
   L->quant_ws = take(nvfp4_quantize_workspace_size(1));
   L->gemm_ws = take(moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H));
+  L->small_scratch = small_layer_eligible(T, E, k, H, I) ? take(small_layer_scratch_bytes(T, k, H)) : SIZE_MAX;
   L->padded_rows = P;
   L->total = o;
   return MOE_OK;
+}
+
+// The single-launch path (small_layer.cu) serves small layers fed logits,
+// unless debug flag bit 2 keeps the staged kernels.
+namespace {
+bool use_small_layer(int T, int E, int k, int H, int I) {
+  return small_layer_eligible(T, E, k, H, I) && (gemm_debug_flags() & 4) == 0;
+}
+}  // namespace
+
+extern "C" int moe_forward_kernel_count(int T, int E, int k, int H, int I) {
+  if (T < 1 || E < 1 || k < 1 || k > E || H < 1 || I < 1) return 0;
+  if (use_small_layer(T, E, k, H, I)) return 1;
+  // routing (one kernel when every item fits one chunk, else top-k, scan and scatter), the
+  // activation amax and quantiser, the two GEMMs, and the FINALIZE closing pass
+  return (route_one_chunk(T, E, k) ? 1 : 3) + 2 + 2 + 1;
 }
 
 extern "C" size_t moe_forward_workspace_size(int T, int E, int k, int H, int I) {
@@ -87,6 +113,7 @@ moe_status forward_check(const uint16_t* x, const float* logits, const moe_weigh
 // steps leave the chain: the activation quantiser's amax pass runs beside the
 // routing (it reads only x), and the FINALIZE accumulator is cleared beside the
 // gate_up GEMM; jev[0..3] are the events of those forks and joins.
+// `external` is set while the layer is being captured into a graph.
 moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t* w_gate, const moe_weights* w,
                           int T, int E, int k, int H, int I, float h_scale, uint16_t* out, void* ws,
                           const moe_forward_layout& L, cudaStream_t stream, cudaEvent_t* ev, bool external,
@@ -120,6 +147,14 @@ moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t
   const bool amax_beside = par && !w_gate;  // with w_gate the router's GEMM supplies x's multiplier
   moe_status s = mark(0);
   if (s != MOE_OK) return s;
+  if (!w_gate && L.small_scratch != SIZE_MAX && use_small_layer(T, E, k, H, I)) {
+    // the whole layer in one launch (its time is all in the first stage); its ticket word is cleared
+    // before eager calls, and a captured replay finds it as the eager pass before the capture left it
+    s = small_layer_enqueue(x, logits, w, T, E, k, H, I, h_scale, out, topk_id, topk_w, offs, p2e, e2p, e2r,
+                            x_scale, x_codes, x_sf, hs, h_codes, h_sf, at(L.small_scratch), !external, stream);
+    for (int i = 1; i <= 4 && s == MOE_OK; ++i) s = mark(i);
+    return s;
+  }
   if (amax_beside) {
     if ((s = fork(jev[0], stream, side)) != MOE_OK) return s;
     s = quantize_amax_enqueue(x, MOE_IN_BF16, T, H, 1, static_cast<uint32_t*>(at(L.quant_ws)), side);

@@ -235,16 +235,6 @@ MOE_DEVINL bool epi_any(int g, bool pred) {
   return r != 0;
 }
 
-// h = silu(g) * u = g / (1 + e^-g) * u in FP32 with the fast hardware forms:
-// __expf (the SFU's 2^x, error growing with |g|) and __fdividef (about 2 ulp),
-// then a correctly rounded product.  Against the FP64 reference on the
-// full-size layers, these flip 16 of 524,288 sampled requantised h codes (one
-// grid step each, at rounding boundaries) in one of nine configurations and none
-// in the other eight; correctly rounded division and expf flip none there, but
-// cost the prefill gate_up launch about a quarter of its time (its epilogue
-// shares the SM with the MMA issue).  For g below about -88 the quotient is -0,
-// the limit of silu there.
-MOE_DEVINL float silu_mul(float g, float u) { return __fmul_rn(__fdividef(g, 1.0f + __expf(-g)), u); }
 
 // ---- epilogue bodies of one 32-column accumulator chunk (shared by both kernels) ----
 // r: the chunk as loaded by tcgen05.ld (this thread's weight row, 32 routed rows);

@@ -43,9 +43,6 @@ inline RouteDims route_dims(int T, int E, int k) {
   return d;
 }
 
-// Larger of two (value, index) candidates: higher value, then lower index.
-MOE_DEVINL bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
-
 // Logits given as FP32 partial sums over K ranges (the router's split GEMM):
 // logit[t][e] = sum over s, in order, of part[t / 128][s][t % 128][e].
 struct PartialLogits {
@@ -108,31 +105,13 @@ MOE_DEVINL void route_tokens(const float* __restrict__ logits, const RouteDims& 
           if (lane + 32 * i < d.E) pl.logits_out[static_cast<int64_t>(t) * d.E + lane + 32 * i] = v[i];
       }
     }
-    float my_v = 0.0f;
-    int my_i = 0;
-    for (int j = 0; j < d.k; ++j) {
-      float bv = -__int_as_float(0x7f800000);
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (!(taken >> i & 1u) && better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == j) { my_v = bv; my_i = bi; }
-    }
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
-    float ex = (lane < d.k) ? route_exp(__fsub_rn(my_v, m)) : 0.0f;
-    float sum = 0.0f;
-    for (int j = 0; j < d.k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, ex, j));
+    int my_i;
+    float my_w;
+    warp_topk_softmax<NV>(v, taken, d.k, &my_i, &my_w);
     if (lane < d.k) {
       int64_t o = static_cast<int64_t>(t) * d.k + lane;
       topk_id[o] = my_i;
-      topk_w[o] = __fdiv_rn(ex, sum);
+      topk_w[o] = my_w;
       atomicAdd(&hist[my_i], 1);
     }
   }
@@ -261,8 +240,9 @@ __global__ void __launch_bounds__(kRouteThreads) scatter_kernel(RouteDims d, con
   const int64_t i1 = min(static_cast<int64_t>(d.T) * d.k, i0 + static_cast<int64_t>(d.chunk_tokens) * d.k);
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) cnt[e] = 0;
   const int64_t i = i0 + threadIdx.x;
-  const bool valid = i < i1;
-  const int e = valid ? topk_id[i] : -1;
+  const int e_in = i < i1 ? topk_id[i] : -1;
+  const bool valid = e_in >= 0 && e_in < d.E;  // an expert id out of range is never placed
+  const int e = valid ? e_in : -1;
   const unsigned active = __ballot_sync(0xffffffffu, valid);
   unsigned peers = 0;
   if (valid) peers = __match_any_sync(active, e);
@@ -355,6 +335,9 @@ extern "C" size_t moe_route_permute_workspace_size(int T, int E, int k) {
 }
 
 namespace moe {
+// True when routing T tokens takes one launch (every item fits one chunk).
+bool route_one_chunk(int T, int E, int k) { return route_dims(T, E, k).n_chunks == 1; }
+
 // Padded offsets live right after the chunk counts in the routing workspace.
 int32_t* route_pad_offsets(void* ws, int T, int E, int k) {
   RouteDims d = route_dims(T, E, k);

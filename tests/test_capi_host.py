@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.moe_abi_version() == 5
+    assert L.moe_abi_version() == 6
     for s in range(8):
         assert L.moe_status_string(s)
     assert L.moe_status_string(99) == b"unknown status"
@@ -62,6 +62,32 @@ def test_forward_layout_is_consistent(L):
     assert lay.x_sf - lay.x_codes >= lay.padded_rows * 6144 // 2
     assert lay.total == L.moe_forward_workspace_size(1024, 256, 8, 6144, 2048)
     assert L.moe_forward_workspace_layout(4, 8, 9, 256, 128, ctypes.byref(lay)) == INVALID  # k > E
+    # the single-launch path's scratch exists only for the small layers it takes
+    SIZE_MAX = 2 ** 64 - 1
+    assert L.moe_forward_workspace_layout(1024, 256, 8, 6144, 2048, ctypes.byref(lay)) == OK
+    assert lay.small_scratch == SIZE_MAX
+    assert L.moe_forward_workspace_layout(16, 8, 2, 256, 128, ctypes.byref(lay)) == OK
+    assert lay.small_scratch != SIZE_MAX and lay.small_scratch % 256 == 0
+    # per-item rows (T * k * H floats) and the ticket word's 256 bytes, inside the workspace
+    assert lay.small_scratch + 16 * 2 * 256 * 4 + 256 <= lay.total == L.moe_forward_workspace_size(16, 8, 2, 256, 128)
+
+
+def test_forward_kernel_count(L):
+    """One launch for the small layers the single-kernel path takes; the staged count otherwise: routing
+    (1 kernel when every item fits one chunk, else 3), amax + quantiser, two GEMMs, the FINALIZE closing
+    pass.  Debug flag bit 2 keeps the staged kernels."""
+    assert L.moe_forward_kernel_count(16, 8, 2, 256, 128) == 1
+    assert L.moe_forward_kernel_count(64, 64, 1, 1024, 512) == 1
+    assert L.moe_forward_kernel_count(33, 8, 2, 256, 128) == 6      # 66 items: staged, one routing chunk
+    assert L.moe_forward_kernel_count(16, 65, 2, 256, 128) == 6     # E > 64
+    assert L.moe_forward_kernel_count(16, 8, 2, 1152, 128) == 6     # H > 1024
+    assert L.moe_forward_kernel_count(1024, 256, 8, 6144, 2048) == 8
+    assert L.moe_forward_kernel_count(16, 8, 9, 256, 128) == 0      # k > E
+    L.moe_debug_set_flags(4)
+    try:
+        assert L.moe_forward_kernel_count(16, 8, 2, 256, 128) == 6
+    finally:
+        L.moe_debug_set_flags(0)
 
 
 def test_blocked_weight_bytes(L):
