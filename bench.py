@@ -542,41 +542,24 @@ def measure_layer(args, T, E, k, H, I, x, logits, pw13, pw2, dev, world, local_r
     if not e2e:
         return res
 
-    # ---- end to end through moe_forward with pinned host buffers
-    # Every step copies its inputs from pinned host memory and reads its output back.  The copies of one
-    # step overlap the layer of the previous one, as a serving pipeline would run them: inputs go in on a
-    # copy stream, the layer runs on the compute stream, the output comes back on a third stream, with two
-    # sets of device buffers (and one graph per set) so a step's copies never touch buffers in use.
+    # ---- end to end through the library's host-buffer call (moe_forward_graph_run_host): every step copies
+    # its inputs from pinned host memory into the graph's device buffers, replays the layer and copies the
+    # output back, all on one stream.  Steps alternate between two streams, each with its own graph, device
+    # buffers and workspace, so one step's copies overlap the other's layer, as a serving pipeline runs.
     xh = x.pin_memory()
     lh = logits.pin_memory()
     ohs = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    fwds = [fwd, moe.MoeForward(T, E, k, H, I, dev)]
     xds = [torch.empty_like(xd) for _ in range(2)]
     lds = [torch.empty_like(ld) for _ in range(2)]
     outs = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    graphs_e2e = [fwd.graph(xds[b], lds[b], pw13, pw2, h_scale, out=outs[b], stage_events=False) for b in range(2)]
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer set b are on the device
-    ev_done = [torch.cuda.Event() for _ in range(2)]    # the layer on buffer set b has finished
-    ev_out = [torch.cuda.Event() for _ in range(2)]     # the output of buffer set b is back on the host
-    for b in range(2):
-        ev_done[b].record(stream)
-        ev_out[b].record(stream)
+    graphs_e2e = [fwds[b].graph(xds[b], lds[b], pw13, pw2, h_scale, out=outs[b], stage_events=False)
+                  for b in range(2)]
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
 
     def e2e_step(i):
         b = i & 1
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_done[b])                  # the layer two steps back has read these inputs
-            xds[b].copy_(xh, non_blocking=True)
-            lds[b].copy_(lh, non_blocking=True)
-            ev_in[b].record(s_in)
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_out[b])                     # the output two steps back has been read
-        graphs_e2e[b].launch()
-        ev_done[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_done[b])
-            ohs[b].copy_(outs[b], non_blocking=True)
-            ev_out[b].record(s_out)
+        graphs_e2e[b].run_host(xh, lh, ohs[b], stream=streams[b])
 
     for i in range(args.warmup):
         e2e_step(i)
@@ -585,13 +568,13 @@ def measure_layer(args, T, E, k, H, I, x, logits, pw13, pw2, dev, world, local_r
         torch.distributed.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    stream.wait_event(e0)
-    s_out.wait_event(e0)
+    e0.record(stream)
+    for st_b in streams:
+        st_b.wait_stream(stream)
     for i in range(args.steps):
         e2e_step(i)
-    stream.wait_event(ev_out[(args.steps - 1) & 1])
-    stream.wait_event(ev_in[(args.steps - 1) & 1])
+    for st_b in streams:
+        stream.wait_stream(st_b)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
@@ -601,8 +584,9 @@ def measure_layer(args, T, E, k, H, I, x, logits, pw13, pw2, dev, world, local_r
     e2e_rel = float((ohs[(args.steps - 1) & 1].float() - ref_out).norm() / max(float(ref_out.norm()), 1e-30))
     res["e2e"] = {"value": whole_job_rate(T * args.steps, world, e2e_ms), "unit": "tokens/s",
                   "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2,
-                  "how": "pinned H2D of x and logits, the layer graph, D2H of the output, every step; one step's "
-                         "copies overlap the previous step's layer (separate copy streams, two buffer sets)",
+                  "how": "moe_forward_graph_run_host every step: pinned H2D of x and logits, the layer graph, D2H "
+                         "of the output, on one stream; steps alternate between two streams (two graphs, buffer "
+                         "sets and workspaces), so one step's copies overlap the other's layer",
                   "output_rel_diff_vs_device_run": e2e_rel}
     return res
 

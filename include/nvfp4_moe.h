@@ -459,6 +459,17 @@ MOE_API moe_status moe_forward_graph_create(const uint16_t* x, const float* logi
                                     int stage_events, moe_forward_graph** graph);
 MOE_API moe_status moe_forward_graph_launch(moe_forward_graph* graph, void* stream);
 MOE_API moe_status moe_forward_graph_stage_ms(moe_forward_graph* graph, float* ms);
+
+/* moe_forward_graph_run_host -- one step of the layer from and to HOST memory:
+ * copies x_host (bf16 [T][H]) and logits_host (f32 [T][E]) into the device
+ * buffers the graph was created with, replays the graph, and copies its output
+ * into out_host (bf16 [T][H]), all enqueued on `stream` (asynchronous: the host
+ * buffers must stay valid and unmodified until the stream reaches the end of
+ * the call; page-locked buffers let the copies overlap other streams' work).
+ * Two graphs, each with its own x, logits, out and workspace, can run steps
+ * on two streams so that one step's copies overlap the other's layer. */
+MOE_API moe_status moe_forward_graph_run_host(moe_forward_graph* graph, const uint16_t* x_host, const float* logits_host,
+                                              uint16_t* out_host, void* stream);
 MOE_API void moe_forward_graph_destroy(moe_forward_graph* graph);
 
 #ifdef __cplusplus

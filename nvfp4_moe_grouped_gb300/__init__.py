@@ -373,6 +373,17 @@ class ForwardGraph:
         _check("moe_forward_graph_launch", _L().moe_forward_graph_launch(self.handle, _stream(stream)))
         return self.out
 
+    def run_host(self, x_host, logits_host, out_host, stream=None):
+        """One step from and to host tensors (page-locked for overlap): copy in, replay, copy out, all on
+        `stream`; returns out_host (valid once the stream gets there)."""
+        for t in (x_host, logits_host, out_host):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("contiguous host tensors are required")
+        _check("moe_forward_graph_run_host", _L().moe_forward_graph_run_host(
+            self.handle, ctypes.c_void_p(x_host.data_ptr()), ctypes.c_void_p(logits_host.data_ptr()),
+            ctypes.c_void_p(out_host.data_ptr()), _stream(stream)))
+        return out_host
+
     def stage_ms(self):
         """(route, quantise, gate_up, down+finalize, total) of the last launch, in ms."""
         ms = (ctypes.c_float * 5)()

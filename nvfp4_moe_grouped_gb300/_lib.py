@@ -84,6 +84,7 @@ SIGNATURES = {
                                          c_void_p, c_void_p, c_size_t, c_int, c_void_p]),
     "moe_forward_graph_launch": (c_int, [c_void_p, c_void_p]),
     "moe_forward_graph_stage_ms": (c_int, [c_void_p, c_void_p]),
+    "moe_forward_graph_run_host": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_forward_graph_destroy": (None, [c_void_p]),
 }
 

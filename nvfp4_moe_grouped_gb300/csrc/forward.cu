@@ -236,6 +236,11 @@ struct moe_forward_graph {
   cudaGraphExec_t exec = nullptr;
   cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   bool timed = false;
+  // the device buffers the graph was captured with, for moe_forward_graph_run_host
+  void* x = nullptr;
+  void* logits = nullptr;
+  void* out = nullptr;
+  size_t x_bytes = 0, logits_bytes = 0, out_bytes = 0;
 };
 
 namespace {
@@ -259,6 +264,12 @@ extern "C" moe_status moe_forward_graph_create(const uint16_t* x, const float* l
   if (!device_error_word() || num_sms() < 1) return MOE_ERR_CUDA;
   moe_forward_graph* g = new moe_forward_graph();
   g->timed = stage_events != 0;
+  g->x = const_cast<uint16_t*>(x);
+  g->logits = const_cast<float*>(logits);
+  g->out = out;
+  g->x_bytes = static_cast<size_t>(T) * H * sizeof(uint16_t);
+  g->logits_bytes = static_cast<size_t>(T) * E * sizeof(float);
+  g->out_bytes = static_cast<size_t>(T) * H * sizeof(uint16_t);
   cudaStream_t st = nullptr, side = nullptr;
   cudaEvent_t jev[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaGraph_t raw = nullptr;
@@ -308,6 +319,19 @@ extern "C" moe_status moe_forward_graph_create(const uint16_t* x, const float* l
 extern "C" moe_status moe_forward_graph_launch(moe_forward_graph* graph, void* stream) {
   if (!graph || !graph->exec) return MOE_ERR_INVALID_ARG;
   return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status moe_forward_graph_run_host(moe_forward_graph* graph, const uint16_t* x_host,
+                                                 const float* logits_host, uint16_t* out_host, void* stream) {
+  if (!graph || !graph->exec || !x_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(graph->x, x_host, graph->x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(graph->logits, logits_host, graph->logits_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaGraphLaunch(graph->exec, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(out_host, graph->out, graph->out_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 extern "C" moe_status moe_forward_graph_stage_ms(moe_forward_graph* graph, float* ms) {

@@ -16,9 +16,11 @@
 // The routing kernel adds the partials in split order (deterministic) as it
 // reads each token's logits, so the logits never make a round trip of their
 // own.  Roles in the GEMM CTA: lane 0 of warp 0 issues the TMA loads (128-byte
-// swizzle, rows past T or E read as zeros), lane 0 of warp 1 the MMAs, warp 2
-// (when asked) takes max |x| over the x tiles for the activation quantiser;
-// all four warps then drain the accumulator.  Every wait is bounded.
+// swizzle, rows past T or E read as zeros), lane 0 of warp 1 the MMAs, warps 2
+// and 3 (when asked) take max |x| over the x tiles for the activation
+// quantiser, half of each stage each, two |bf16| patterns per 32-bit word
+// (one warp taking them one by one held the mainloop to its pace); all four
+// warps then drain the accumulator.  Every wait is bounded.
 #include "common.cuh"
 
 namespace moe {
@@ -66,8 +68,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   const bool amax_on = p.amax_bits != nullptr;
   if (threadIdx.x == 0) {
-    // a stage is free once the MMAs and (when x's amax is wanted) warp 2 are done with it
-    for (int s = 0; s < kRStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], amax_on ? 2 : 1); }
+    // a stage is free once the MMAs and (when x's amax is wanted) warps 2 and 3 are done with it
+    for (int s = 0; s < kRStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], amax_on ? 3 : 1); }
     mbar_init(acc_full, 1);
     *s_abort = 0;
     fence_barrier_init();
@@ -123,10 +125,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
       mma_commit(&empty[s]);
     }
     mma_commit(acc_full);  // arrives once every MMA issued above has completed
-  } else if (warp == 2 && amax_on) {
+  } else if ((warp == 2 || warp == 3) && amax_on) {
     // ---- max |x| over this CTA's x tiles (each x element is in exactly one CTA's tiles; rows past T
-    // are zero-filled), for the NVFP4 decode multiplier of the activation quantiser ----
-    uint32_t m = 0;  // max of |bf16| bit patterns: the order of non-negative values
+    // are zero-filled), for the NVFP4 decode multiplier of the activation quantiser: warp 2 the first
+    // half of every stage, warp 3 the second; |bf16| bit patterns order like the values ----
+    const int hw = warp - 2;
+    uint32_t m2 = 0;  // maxima of the two halfwords
     for (int i = 0; i < nk; ++i) {
       const int s = i % kRStages;
       const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
@@ -138,17 +142,19 @@ __global__ void __launch_bounds__(kRThreads, 1)
         }
         break;
       }
-      const uint4* a4 = reinterpret_cast<const uint4*>(s_a + s * kRAStage);
-#pragma unroll 4
-      for (int j = lane; j < kRAStage / 16; j += 32) {
+      const uint4* a4 = reinterpret_cast<const uint4*>(s_a + s * kRAStage + hw * (kRAStage / 2));
+#pragma unroll 8
+      for (int j = lane; j < kRAStage / 32; j += 32) {
         const uint4 u = a4[j];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+        m2 = __vmaxu2(m2, u.x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, u.y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, u.z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, u.w & 0x7FFF7FFFu);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0 && m > 0) atomicMax(p.amax_bits, m << 16);  // the bf16 pattern as an f32 pattern
