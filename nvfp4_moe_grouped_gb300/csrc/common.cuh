@@ -94,8 +94,18 @@ MOE_DEVINL float route_exp(float x) {
   return __fmul_rn(p, two_n);
 }
 
-// Larger of two (value, index) routing candidates: higher value, then lower index.
-MOE_DEVINL bool route_better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+// Routing order of a logit as an unsigned integer: larger logits give larger
+// codes, -0 and +0 the same one, and every non-NaN logit a code above 0, so 0
+// can stand for "not a candidate".
+MOE_DEVINL uint32_t route_order_bits(float x) {
+  const uint32_t b = x == 0.0f ? 0u : __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The logit a routing code stands for (+0 for either zero).
+MOE_DEVINL float route_order_value(uint32_t ob) {
+  return __uint_as_float((ob & 0x80000000u) ? (ob & 0x7FFFFFFFu) : ~ob);
+}
 
 // Top-k and softmax of one token whose E logits a warp holds: lane l owns
 // experts l + 32 i in v[i], and bit i of `taken` is set where that expert does
@@ -103,26 +113,33 @@ MOE_DEVINL bool route_better(float v, int i, float bv, int bi) { return v > bv |
 // lane j: *id its expert, *w its weight, the softmax of the k selected logits
 // (exponentials of the differences to the largest, summed in slot order, one
 // correctly rounded division).  Lanes >= k get *w = 0 and an unspecified *id.
+// Each of the k rounds takes the largest remaining code with one warp max
+// reduction and, among the experts holding it, the lowest index with one warp
+// min reduction; the winner's code is then cleared.  NaN logits are not
+// supported (their order is unspecified).
 template <int NV>
 MOE_DEVINL void warp_topk_softmax(const float (&v)[NV], uint32_t taken, int k, int* id, float* w) {
   const int lane = threadIdx.x & 31;
-  float my_v = 0.0f;
+  uint32_t ob[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) ob[i] = (taken >> i & 1u) ? 0u : route_order_bits(v[i]);
+  uint32_t my_ob = 0u;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -__int_as_float(0x7f800000);
-    int bi = 0x7fffffff;
+    uint32_t lm = ob[0];
 #pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (!(taken >> i & 1u) && route_better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
+    for (int i = 1; i < NV; ++i) lm = max(lm, ob[i]);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, lm);
+    int ci = NV;  // this lane's lowest slot holding the maximum
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (route_better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) { my_v = bv; my_i = bi; }
+    for (int i = NV - 1; i >= 0; --i) ci = ob[i] == m ? i : ci;
+    const int bi = __reduce_min_sync(0xffffffffu, ci < NV ? lane + 32 * ci : 0x7fffffff);
+    const int bd = bi - lane;  // 32 i in the winner's lane, not a multiple of 32 in the others
+#pragma unroll
+    for (int i = 0; i < NV; ++i) ob[i] = bd == 32 * i ? 0u : ob[i];
+    if (lane == j) { my_ob = m; my_i = bi; }
   }
+  const float my_v = route_order_value(my_ob);
   const float m = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = (lane < k) ? route_exp(__fsub_rn(my_v, m)) : 0.0f;
   float sum = 0.0f;

@@ -55,22 +55,39 @@ struct PartialLogits {
 
 // Top-k and softmax of tokens [t0, t1), one warp per token (warps of the whole
 // block in turn); counts each selected expert in the shared histogram `hist`.
-// BATCH (partial sums, NV <= 8, at most kMaxSplits splits): all loads first.
+// Plain logits (E <= 256): a warp loads its next token's row while it ranks
+// the current one.  BATCH (partial sums, NV <= 8, at most kMaxSplits splits): all loads
+// first.
 template <int NV, bool PARTS, bool BATCH = false>  // NV: logits per lane, NV * 32 >= E; PARTS: read partial sums
 MOE_DEVINL void route_tokens(const float* __restrict__ logits, const RouteDims& d, int t0, int t1,
                              int32_t* __restrict__ topk_id, float* __restrict__ topk_w, int* hist,
                              const PartialLogits& pl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int t = t0 + warp; t < t1; t += blockDim.x / 32) {
-    const float* row = logits + static_cast<int64_t>(t) * d.E;
-    float v[NV];
-    uint32_t taken = 0;
+  const int nw = blockDim.x / 32;
+  uint32_t taken = 0;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      int e = lane + 32 * i;
-      v[i] = 0.0f;
-      if (e >= d.E) taken |= 1u << i;
-      else if (!PARTS) v[i] = __ldg(row + e);
+  for (int i = 0; i < NV; ++i)
+    if (lane + 32 * i >= d.E) taken |= 1u << i;
+  constexpr bool kAhead = !PARTS && NV <= 8;
+  float nxt[NV];  // plain logits: the row of the warp's next token
+  if (kAhead) {
+    const float* row = logits + static_cast<int64_t>(t0 + warp < t1 ? t0 + warp : t0) * d.E;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) nxt[i] = (t0 + warp < t1 && !(taken >> i & 1u)) ? __ldg(row + lane + 32 * i) : 0.0f;
+  }
+  for (int t = t0 + warp; t < t1; t += nw) {
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = kAhead ? nxt[i] : 0.0f;
+    if (!PARTS && !kAhead) {
+      const float* row = logits + static_cast<int64_t>(t) * d.E;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = (taken >> i & 1u) ? 0.0f : __ldg(row + lane + 32 * i);
+    }
+    if (kAhead && t + nw < t1) {
+      const float* row = logits + static_cast<int64_t>(t + nw) * d.E;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) nxt[i] = (taken >> i & 1u) ? 0.0f : __ldg(row + lane + 32 * i);
     }
     if (PARTS && BATCH) {
       // every partial sum of the lane's experts loaded at once, then added in split order
@@ -126,7 +143,9 @@ MOE_DEVINL void router_x_scale(const PartialLogits& pl) {
 }
 
 template <int NV, bool PARTS, bool BATCH = false>
-__global__ void __launch_bounds__(BATCH ? kPartsThreads : kTopkThreads) route_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(PARTS ? (BATCH ? kPartsThreads : kTopkThreads) : kRouteThreads,
+                                  PARTS || NV > 8 ? 1 : 4)
+    route_kernel(const float* __restrict__ logits,
                                                                                    RouteDims d,
                                                               int32_t* __restrict__ topk_id,
                                                               float* __restrict__ topk_w,
@@ -172,73 +191,121 @@ MOE_DEVINL int block_exclusive_scan(int v, int* warp_tot) {
   return r;
 }
 
-// One block of 1024 threads: thread (g, e) = (tid / Ep, tid % Ep), Ep = E rounded
-// up to 32, covers chunk group g of expert e (G = 1024 / Ep groups split the
-// chunks), so up to G loads per expert are in flight instead of one.
-__global__ void __launch_bounds__(1024) scan_kernel(RouteDims d, int32_t* __restrict__ chunk_counts,
-                                                     int32_t* __restrict__ expert_offsets,
-                                                     int32_t* __restrict__ pad_offsets) {
-  __shared__ int warp_tot[32];
-  __shared__ int part[1024];  // [G][Ep] per-group totals, then per-group bases
-  const int Ep = (d.E + 31) & ~31;
-  const int G = blockDim.x / Ep;
-  const int g = threadIdx.x / Ep, e = threadIdx.x - g * Ep;
-  const bool act = g < G && e < d.E;
-  const int b0 = act ? static_cast<int>(static_cast<int64_t>(g) * d.n_chunks / G) : 0;
-  const int b1 = act ? static_cast<int>(static_cast<int64_t>(g + 1) * d.n_chunks / G) : 0;
+// Each expert's items before every chunk: chunk_counts[b][e] (items of expert e
+// in chunk b) becomes the exclusive prefix over chunks b' < b, and
+// expert_total[e] the sum over all chunks.  Block x covers the 32 experts
+// 32 x .. 32 x + 31 (one per lane, so a warp reads 128 contiguous bytes of a
+// chunk's row) and splits the chunks into 32 groups, one per warp; the group
+// sums are scanned per expert in shared memory, then every thread rewrites its
+// chunks from its group's base.  The expert offsets themselves (a scan over
+// experts) are left to the scatter.
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(RouteDims d, int32_t* __restrict__ chunk_counts,
+                                                          int32_t* __restrict__ expert_total) {
+  __shared__ int part[32][33];  // [group][expert of the block], then each group's base
+  constexpr int kB = 8;         // loads issued together
+  const int g = threadIdx.x >> 5, c = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + c;
+  const bool act = e < d.E;
+  const int b0 = static_cast<int>(static_cast<int64_t>(g) * d.n_chunks / 32);
+  const int b1 = static_cast<int>(static_cast<int64_t>(g + 1) * d.n_chunks / 32);
   int sub = 0;
-#pragma unroll 8
-  for (int b = b0; b < b1; ++b) sub += chunk_counts[static_cast<int64_t>(b) * d.E + e];
-  if (g < G) part[threadIdx.x] = sub;
+  if (act) {
+    for (int b = b0; b < b1; b += kB) {
+      int v[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) v[u] = b + u < b1 ? chunk_counts[static_cast<int64_t>(b + u) * d.E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < kB; ++u) sub += v[u];
+    }
+  }
+  part[g][c] = sub;
   __syncthreads();
-  // group 0 holds each expert's total; thread order puts group 0 first, so the
-  // block-wide exclusive scan over (group 0 totals, zeros) gives the expert offsets
-  int total = 0;
-  if (g == 0 && e < d.E)
-    for (int h = 0; h < G; ++h) total += part[h * Ep + e];
-  const int off = block_exclusive_scan(total, warp_tot);
-  const int padded = (g == 0 && e < d.E) ? ((total + 127) / 128) * 128 : 0;
-  const int poff = block_exclusive_scan(padded, warp_tot);
-  if (g == 0 && e < d.E) {
-    expert_offsets[e] = off;
-    pad_offsets[e] = poff;
-    if (e == d.E - 1) {
-      expert_offsets[d.E] = off + total;
-      pad_offsets[d.E] = poff + padded;
+  {  // warp g scans expert 32 x + g over the groups: lane c holds group c
+    const int v = part[c][g];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (c >= o) x += y;
     }
-    // per-group bases of this expert
-    int run = off;
-    for (int h = 0; h < G; ++h) {
-      const int c = part[h * Ep + e];
-      part[h * Ep + e] = run;
-      run += c;
-    }
+    part[c][g] = x - v;
+    const int eg = blockIdx.x * 32 + g;
+    if (c == 31 && eg < d.E) expert_total[eg] = x;
   }
   __syncthreads();
   if (act) {
-    int run = part[threadIdx.x];
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) {
-      const int64_t o = static_cast<int64_t>(b) * d.E + e;
-      const int c = chunk_counts[o];
-      chunk_counts[o] = run;  // becomes the chunk's first position for expert e
-      run += c;
+    int run = part[g][c];
+    for (int b = b0; b < b1; b += kB) {
+      int v[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) v[u] = b + u < b1 ? chunk_counts[static_cast<int64_t>(b + u) * d.E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        if (b + u < b1) chunk_counts[static_cast<int64_t>(b + u) * d.E + e] = run;
+        run += v[u];
+      }
     }
   }
 }
 
+// Expert offsets and 128-row padded offsets from the per-expert totals, into
+// shared `off` and `poff` (every block of the scatter computes them; block 0
+// also writes them out, with the grand totals at index E).  256 threads, each
+// over up to four consecutive experts (E <= 1024).
+MOE_DEVINL void expert_offsets_from_totals(const RouteDims& d, const int32_t* __restrict__ expert_total, int* off,
+                                           int* poff, int* warp_tot, int32_t* __restrict__ expert_offsets,
+                                           int32_t* __restrict__ pad_offsets) {
+  const int per = (d.E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = threadIdx.x * per;
+  int tot[4], s = 0, ps = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    tot[u] = (u < per && e0 + u < d.E) ? expert_total[e0 + u] : 0;
+    s += tot[u];
+    ps += (tot[u] + 127) / 128 * 128;
+  }
+  int o = block_exclusive_scan(s, warp_tot);
+  int po = block_exclusive_scan(ps, warp_tot);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (u < per && e0 + u < d.E) {
+      off[e0 + u] = o;
+      poff[e0 + u] = po;
+      if (blockIdx.x == 0) {
+        expert_offsets[e0 + u] = o;
+        pad_offsets[e0 + u] = po;
+      }
+      o += tot[u];
+      po += (tot[u] + 127) / 128 * 128;
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == kRouteThreads - 1) {  // past the last expert: the grand totals
+    expert_offsets[d.E] = o;
+    pad_offsets[d.E] = po;
+  }
+}
+
+// Stable scatter of one chunk of items: item i = t * k + j of expert e goes to
+// position off[e] + (items of e in earlier chunks) + (items of e before it in
+// this chunk), warps in order and peers by lane.
 __global__ void __launch_bounds__(kRouteThreads) scatter_kernel(RouteDims d, const int32_t* __restrict__ topk_id,
                                                                 const int32_t* __restrict__ chunk_base,
-                                                                const int32_t* __restrict__ expert_offsets,
-                                                                const int32_t* __restrict__ pad_offsets,
+                                                                const int32_t* __restrict__ expert_total,
+                                                                int32_t* __restrict__ expert_offsets,
+                                                                int32_t* __restrict__ pad_offsets,
                                                                 int32_t* __restrict__ perm_to_expanded,
                                                                 int32_t* __restrict__ expanded_to_perm,
                                                                 int32_t* __restrict__ expanded_to_row) {
-  extern __shared__ int cnt[];  // [E] items of each expert seen so far in this chunk
+  extern __shared__ int sm[];
+  int* cnt = sm;             // [E] items of each expert seen so far in this chunk
+  int* off = sm + d.E;       // [E] expert offsets
+  int* poff = sm + 2 * d.E;  // [E] padded expert offsets
+  __shared__ int warp_tot[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t i0 = static_cast<int64_t>(blockIdx.x) * d.chunk_tokens * d.k;
   const int64_t i1 = min(static_cast<int64_t>(d.T) * d.k, i0 + static_cast<int64_t>(d.chunk_tokens) * d.k);
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) cnt[e] = 0;
+  expert_offsets_from_totals(d, expert_total, off, poff, warp_tot, expert_offsets, pad_offsets);
   const int64_t i = i0 + threadIdx.x;
   const int e_in = i < i1 ? topk_id[i] : -1;
   const bool valid = e_in >= 0 && e_in < d.E;  // an expert id out of range is never placed
@@ -254,10 +321,11 @@ __global__ void __launch_bounds__(kRouteThreads) scatter_kernel(RouteDims d, con
       __syncwarp(active);
       int leader = __ffs(peers) - 1;
       if (lane == leader) cnt[e] = base + __popc(peers);
-      int64_t p = static_cast<int64_t>(chunk_base[static_cast<int64_t>(blockIdx.x) * d.E + e]) + base + rank_in_warp;
+      const int within = chunk_base[static_cast<int64_t>(blockIdx.x) * d.E + e] + base + rank_in_warp;
+      const int p = off[e] + within;
       perm_to_expanded[p] = static_cast<int32_t>(i);
-      expanded_to_perm[i] = static_cast<int32_t>(p);
-      expanded_to_row[i] = static_cast<int32_t>(pad_offsets[e] + (p - expert_offsets[e]));
+      expanded_to_perm[i] = p;
+      expanded_to_row[i] = poff[e] + within;
     }
   }
 }
@@ -330,15 +398,16 @@ extern "C" size_t moe_route_permute_workspace_size(int T, int E, int k) {
   if (T < 1 || E < 1 || k < 1) return 0;
   RouteDims d = route_dims(T, E, k);
   size_t counts = static_cast<size_t>(d.n_chunks) * E * sizeof(int32_t);
-  size_t pads = static_cast<size_t>(E + 1) * sizeof(int32_t);
-  return ((counts + 255) / 256) * 256 + ((pads + 255) / 256) * 256;
+  size_t pads = static_cast<size_t>(E + 1) * sizeof(int32_t);  // padded offsets, then each expert's total
+  return ((counts + 255) / 256) * 256 + 2 * (((pads + 255) / 256) * 256);
 }
 
 namespace moe {
 // True when routing T tokens takes one launch (every item fits one chunk).
 bool route_one_chunk(int T, int E, int k) { return route_dims(T, E, k).n_chunks == 1; }
 
-// Padded offsets live right after the chunk counts in the routing workspace.
+// Padded offsets live right after the chunk counts in the routing workspace,
+// each expert's total (E ints, 256-byte aligned) right after them.
 int32_t* route_pad_offsets(void* ws, int T, int E, int k) {
   RouteDims d = route_dims(T, E, k);
   size_t counts = static_cast<size_t>(d.n_chunks) * E * sizeof(int32_t);
@@ -357,6 +426,7 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
   RouteDims d = route_dims(T, E, k);
   int32_t* counts = static_cast<int32_t*>(ws);
   int32_t* pads = route_pad_offsets(ws, T, E, k);
+  int32_t* totals = pads + ((static_cast<size_t>(E + 1) * sizeof(int32_t) + 255) / 256) * 256 / sizeof(int32_t);
   const size_t hist_bytes = sizeof(int) * E;
   const int nv = (E + 31) / 32;
   const PartialLogits pl{part, splits, NE, logits_out, x_amax_bits, x_scale};
@@ -384,7 +454,7 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
                                                     st>>>(logits, d, topk_id, topk_w, counts, pl)                      \
                  : route_kernel<NV, true><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w,    \
                                                                                        counts, pl))                  \
-        : route_kernel<NV, false><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl))
+        : route_kernel<NV, false><<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl))
   if (nv <= 1) MOE_ROUTE(1);
   else if (nv <= 2) MOE_ROUTE(2);
   else if (nv <= 4) MOE_ROUTE(4);
@@ -392,9 +462,10 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
   else if (nv <= 16) MOE_ROUTE(16);
   else MOE_ROUTE(32);
 #undef MOE_ROUTE
-  scan_kernel<<<1, 1024, 0, st>>>(d, counts, expert_offsets, pads);
-  scatter_kernel<<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(d, topk_id, counts, expert_offsets, pads,
-                                                                perm_to_expanded, expanded_to_perm, expanded_to_row);
+  chunk_scan_kernel<<<(E + 31) / 32, 1024, 0, st>>>(d, counts, totals);
+  scatter_kernel<<<d.n_chunks, kRouteThreads, 3 * hist_bytes, st>>>(d, topk_id, counts, totals, expert_offsets, pads,
+                                                                    perm_to_expanded, expanded_to_perm,
+                                                                    expanded_to_row);
   return check_launch();
 }
 }  // namespace moe

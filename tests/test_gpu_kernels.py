@@ -25,16 +25,30 @@ def _tie_logits(T, E, seed):
     return (torch.randint(0, 6, (T, E), generator=g).float() * 0.5).numpy()
 
 
+def _signed_zero_logits(T, E, seed):
+    """Mostly -0.0 and +0.0 (equal logits: the lower index goes first, whatever the sign), some -inf and a few
+    0.5, so the selected sets mix zeros of both signs and the weights see differences of zeros."""
+    g = torch.Generator().manual_seed(seed)
+    vals = torch.tensor([-float("inf"), -0.0, 0.0, 0.5])
+    pick = torch.multinomial(torch.tensor([0.3, 0.33, 0.33, 0.04]), T * E, replacement=True, generator=g)
+    return vals[pick].view(T, E).numpy()
+
+
 # ------------------------------------------------------------------ routing / permutation
 
 @pytest.mark.parametrize("T,E,k,kind", [(16, 8, 2, "normal"), (300, 256, 8, "normal"), (1024, 256, 8, "zipf"),
                                         (5, 64, 3, "normal"), (1, 4, 4, "normal"), (777, 256, 8, "ties"),
-                                        (64, 1000, 32, "normal"), (4096, 256, 8, "normal")])
+                                        (64, 1000, 32, "normal"), (4096, 256, 8, "normal"),
+                                        (500, 256, 8, "zeros"), (100, 1000, 32, "zeros"), (40, 1000, 4, "zeros"),
+                                        (3000, 96, 1, "normal"), (257, 33, 5, "ties")])
 def test_route_permute_bitexact(T, E, k, kind):
     if kind == "zipf":
         logits = inputs.router_logits(T, E, zipf_s=1.1).numpy()
     elif kind == "ties":
         logits = _tie_logits(T, E, 9)
+    elif kind == "zeros":
+        logits = _signed_zero_logits(T, E, 11)
+        assert (np.signbit(logits) & (logits == 0)).any() and ((~np.signbit(logits)) & (logits == 0)).any()
     else:
         logits = inputs.router_logits(T, E, seed=T * 7 + E).numpy()
     ids, w = oracle.route(logits, k)
