@@ -392,22 +392,23 @@ typedef struct {
 typedef struct {
   size_t topk_id, topk_w, expert_offsets, perm_to_expanded, expanded_to_perm, expanded_to_row;
   size_t x_scale, x_codes, x_sf, h_scale, h_codes, h_sf, route_ws, quant_ws, gemm_ws;
-  size_t small_scratch; /* scratch of the single-launch path; (size_t)-1 for layers it does not take */
+  size_t small_scratch; /* 256 bytes reserved for the single-launch path; (size_t)-1 for layers it does not take */
   int64_t padded_rows; /* rows allocated for the routed-row buffers */
   size_t total;
 } moe_forward_layout;
 
-/* Small layers (T * k <= 64, E <= 64, H <= 1024, I <= 512) run as ONE kernel
- * ("Tracing the Failure ...", "Conclusion": persistent kernel designs against
- * per-kernel overheads): one CTA per expert routes every token itself, takes
- * x's amax itself, quantises its rows, runs both contractions on the CUDA cores
- * and writes each routed row times its router weight to small_scratch; the last
- * CTA to finish sums every token's k rows in slot order into `out`.  Every
- * intermediate of the layout is written as the staged kernels write it: the
- * routing and permutation and the quantised x are the same bits, and h and out
- * differ only by the order of the FP32 sums in the contractions.  A ticket word
- * at the end of small_scratch is left at 0 by every launch (moe_forward clears
- * it first; a graph relies on the eager pass of its creation).
+/* Small layers (T * k <= 64, E <= 64, H <= 1024, I <= 512, E * I <= 4096, and
+ * no gate matrix) run as ONE kernel ("Tracing the Failure ...", "Conclusion":
+ * persistent kernel designs against per-kernel overheads): one cluster of 16
+ * CTAs (8 where 16 cannot be placed).  Every CTA routes every token itself and
+ * takes x's amax itself; gate_up, SiLU-mul and the requantisation of h are
+ * dealt out in (expert, 32 h columns) units; after the cluster barrier each CTA
+ * runs down for its share of the output columns over every routed row and sums
+ * each token's k slots in slot order into `out`.  Every intermediate of the
+ * layout is written as the staged kernels write it: the routing and
+ * permutation and the quantised x are the same bits, and h and out differ only
+ * by the order of the FP32 sums in the contractions.  No state carries from one
+ * launch to the next.
  * moe_forward_kernel_count: kernels one moe_forward call (or one replay of its
  * graph) launches for this shape, 0 for an invalid shape. */
 MOE_API int moe_forward_kernel_count(int T, int E, int k, int H, int I);

@@ -12,12 +12,12 @@ namespace moe {
 int32_t* route_pad_offsets(void* ws, int T, int E, int k);
 int& gemm_debug_flags();
 bool small_layer_eligible(int T, int E, int k, int H, int I);
-size_t small_layer_scratch_bytes(int T, int k, int H);
+size_t small_layer_scratch_bytes(int T, int k, int I);
 moe_status small_layer_enqueue(const uint16_t* x, const float* logits, const moe_weights* w, int T, int E, int k,
                                int H, int I, float h_scale, uint16_t* out, int32_t* topk_id, float* topk_w,
                                int32_t* offs, int32_t* p2e, int32_t* e2p, int32_t* e2r, float* x_scale,
                                uint8_t* x_codes, uint8_t* x_sf, float* hs, uint8_t* h_codes, uint8_t* h_sf,
-                               void* scratch, bool clear_ticket, cudaStream_t st);
+                               void* scratch, cudaStream_t st);
 bool route_one_chunk(int T, int E, int k);
 }
 
@@ -48,7 +48,7 @@ extern "C" moe_status moe_forward_workspace_layout(int T, int E, int k, int H, i
   L->route_ws = take(moe_route_permute_workspace_size(T, E, k));
   L->quant_ws = take(nvfp4_quantize_workspace_size(1));
   L->gemm_ws = take(moe_grouped_gemm_workspace_size(MOE_EPI_FINALIZE, T, k, H));
-  L->small_scratch = small_layer_eligible(T, E, k, H, I) ? take(small_layer_scratch_bytes(T, k, H)) : SIZE_MAX;
+  L->small_scratch = small_layer_eligible(T, E, k, H, I) ? take(small_layer_scratch_bytes(T, k, I)) : SIZE_MAX;
   L->padded_rows = P;
   L->total = o;
   return MOE_OK;
@@ -148,10 +148,9 @@ moe_status forward_stages(const uint16_t* x, const float* logits, const uint16_t
   moe_status s = mark(0);
   if (s != MOE_OK) return s;
   if (!w_gate && L.small_scratch != SIZE_MAX && use_small_layer(T, E, k, H, I)) {
-    // the whole layer in one launch (its time is all in the first stage); its ticket word is cleared
-    // before eager calls, and a captured replay finds it as the eager pass before the capture left it
+    // the whole layer in one launch (its time is all in the first stage)
     s = small_layer_enqueue(x, logits, w, T, E, k, H, I, h_scale, out, topk_id, topk_w, offs, p2e, e2p, e2r,
-                            x_scale, x_codes, x_sf, hs, h_codes, h_sf, at(L.small_scratch), !external, stream);
+                            x_scale, x_codes, x_sf, hs, h_codes, h_sf, at(L.small_scratch), stream);
     for (int i = 1; i <= 4 && s == MOE_OK; ++i) s = mark(i);
     return s;
   }

@@ -68,8 +68,8 @@ def test_forward_layout_is_consistent(L):
     assert lay.small_scratch == SIZE_MAX
     assert L.moe_forward_workspace_layout(16, 8, 2, 256, 128, ctypes.byref(lay)) == OK
     assert lay.small_scratch != SIZE_MAX and lay.small_scratch % 256 == 0
-    # per-item rows (T * k * H floats) and the ticket word's 256 bytes, inside the workspace
-    assert lay.small_scratch + 16 * 2 * 256 * 4 + 256 <= lay.total == L.moe_forward_workspace_size(16, 8, 2, 256, 128)
+    # 256 reserved bytes inside the workspace
+    assert lay.small_scratch + 256 <= lay.total == L.moe_forward_workspace_size(16, 8, 2, 256, 128)
 
 
 def test_forward_kernel_count(L):
@@ -77,7 +77,9 @@ def test_forward_kernel_count(L):
     (1 kernel when every item fits one chunk, else 3), amax + quantiser, two GEMMs, the FINALIZE closing
     pass.  Debug flag bit 2 keeps the staged kernels."""
     assert L.moe_forward_kernel_count(16, 8, 2, 256, 128) == 1
-    assert L.moe_forward_kernel_count(64, 64, 1, 1024, 512) == 1
+    assert L.moe_forward_kernel_count(64, 8, 1, 1024, 512) == 1      # T * k, H, I and E * I at their limits
+    assert L.moe_forward_kernel_count(64, 64, 1, 256, 64) == 1       # E at its limit
+    assert L.moe_forward_kernel_count(64, 64, 1, 1024, 512) == 6     # E * I > 4096: staged
     assert L.moe_forward_kernel_count(33, 8, 2, 256, 128) == 6      # 66 items: staged, one routing chunk
     assert L.moe_forward_kernel_count(16, 65, 2, 256, 128) == 6     # E > 64
     assert L.moe_forward_kernel_count(16, 8, 2, 1152, 128) == 6     # H > 1024
