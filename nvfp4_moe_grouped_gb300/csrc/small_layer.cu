@@ -152,29 +152,40 @@ MOE_DEVINL void chunk_fma(const Chunk& t, int q, const float* v, int ld, int R, 
   block16_fma(t.c.z, t.c.w, chunk_scale(t, q, 1), v + 16, ld, R, acc);
 }
 
+// Eight e2m1 codes (a 32-bit word, element j in bits 4j..4j+3) as four f16x2
+// pairs (the hardware conversion, exact; the even element in the low half).
+MOE_DEVINL void e2m1x8_to_h2x4(uint32_t w, __half2 (&h)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 q;\n\tcvt.u8.u32 q, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, q;\n\t}" : "=r"(h2) : "r"((w >> (8 * j)) & 0xFFu));
+    h[j] = *reinterpret_cast<const __half2*>(&h2);
+  }
+}
+
 // acc + the dot product of chunk t of a weight row with the 32 h elements of
 // the same K range: hc their e2m1 codes (element j in bits 4j.. of the byte
 // string), hsf the four h block scales of the chunk's 64-element K-step.  Per
-// 16-element block: (sum of exact e2m1 x e2m1 products) x h scale x weight
-// scale.
+// 16-element block: (sum of the e2m1 x e2m1 products) x h scale x weight
+// scale.  The products (at most 36 in magnitude, multiples of 1/4) and their
+// sums over eight elements (at most 288) are exact in f16, so the block sum is
+// taken with packed f16x2 multiply-adds, each half over eight products, and the
+// two halves are added in FP32: the exact sum, as an FP32 chain would give it.
 MOE_DEVINL float chunk_dot_codes(const Chunk& t, int q, const uint4& hc, uint32_t hsf, float acc) {
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
-    const uint32_t wlo = b ? t.c.z : t.c.x, whi = b ? t.c.w : t.c.y;
-    const uint32_t hlo = b ? hc.z : hc.x, hhi = b ? hc.w : hc.y;
-    float part = 0.0f;
+    __half2 w[4], h[4];
+    __half2 s2 = __float2half2_rn(0.0f);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 wa = e2m1x2_to_f32x2((wlo >> (8 * j)) & 0xFFu), ha = e2m1x2_to_f32x2((hlo >> (8 * j)) & 0xFFu);
-      part = __fmaf_rn(wa.x, ha.x, part);
-      part = __fmaf_rn(wa.y, ha.y, part);
-    }
+    for (int half8 = 0; half8 < 2; ++half8) {
+      const uint32_t ww = b ? (half8 ? t.c.w : t.c.z) : (half8 ? t.c.y : t.c.x);
+      const uint32_t hw = b ? (half8 ? hc.w : hc.z) : (half8 ? hc.y : hc.x);
+      e2m1x8_to_h2x4(ww, w);
+      e2m1x8_to_h2x4(hw, h);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 wa = e2m1x2_to_f32x2((whi >> (8 * j)) & 0xFFu), ha = e2m1x2_to_f32x2((hhi >> (8 * j)) & 0xFFu);
-      part = __fmaf_rn(wa.x, ha.x, part);
-      part = __fmaf_rn(wa.y, ha.y, part);
+      for (int j = 0; j < 4; ++j) s2 = __hfma2(w[j], h[j], s2);
     }
+    const float part = __fadd_rn(__low2float(s2), __high2float(s2));
     const float hs = e4m3_decode((hsf >> (16 * (q & 1) + 8 * b)) & 0xFFu);
     acc = __fmaf_rn(__fmul_rn(hs, chunk_scale(t, q, b)), part, acc);
   }
@@ -481,8 +492,22 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_layer_kernel(const Sma
     }
   }
 
-  // ---- 4. every item's quantised h is written: the cluster barrier publishes it to every CTA
-  cluster_sync_all();
+  // ---- 4. every item's quantised h is written: the cluster barrier publishes it to every CTA.  Between
+  // its arrive and its wait each thread requests the first four K chunks of its first down row (they do
+  // not depend on phase 1), so only the h loads follow the barrier.
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  Chunk w2first[4];
+  float w2s_first = 0.0f;
+  if (tid < n_items * Hc) {
+    const int item = tid / Hc, n = c * Hc + (tid - (tid / Hc) * Hc);
+    const uint8_t* blk =
+        p.w2 + (static_cast<int64_t>(s_id[item]) * mt2 + (n >> 7)) * kt2 * kBlockedTileBytes;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < I / 32) load_chunk(blk, n & 127, j, w2first[j]);
+    w2s_first = __ldg(p.w2_scale + s_id[item]);
+  }
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 
   // ---- 5. phase 2: down + FINALIZE for output columns [c Hc, c Hc + Hc): one thread per (item, column),
   // four K chunks of the weight row and of the item's h row requested together
@@ -501,7 +526,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_layer_kernel(const Sma
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (q0 + j < I / 32) {
-          load_chunk(blk, n & 127, q0 + j, t[j]);
+          if (q == tid && q0 == 0) t[j] = w2first[j];
+          else load_chunk(blk, n & 127, q0 + j, t[j]);
           hc[j] = __ldcg(hcodes + q0 + j);
         }
       }
@@ -513,7 +539,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) small_layer_kernel(const Sma
       for (int j = 0; j < 4; ++j)
         if (q0 + j < I / 32) acc = chunk_dot_codes(t[j], q0 + j, hc[j], hsf[j >> 1], acc);
     }
-    const float alpha2 = __fmul_rn(p.h_scale, __ldg(p.w2_scale + e));
+    const float alpha2 = __fmul_rn(p.h_scale, q == tid ? w2s_first : __ldg(p.w2_scale + e));
     s_y[q] = __fmul_rn(__fmul_rn(s_w[item], alpha2), acc);
   }
   __syncthreads();
