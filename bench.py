@@ -923,8 +923,8 @@ def run_gated(args, rank, world, local_rank):
                        "l2": "weights exceed L2; no flush" if flush is None else "256 MB written between steps"},
             "roofline": roof,
             "same_layer_fed_logits_ms": ms_plain,
-            # router GEMM, routing (3), quantiser, gate_up, down, FP32->BF16 per step
-            "gpu_launches": 8 * args.steps, "clocks": clk.summary()}), flush=True)
+            # router (logits GEMM + top-k), scan, scatter, quantiser, gate_up, down, FP32->BF16 per step
+            "gpu_launches": 7 * args.steps, "clocks": clk.summary()}), flush=True)
 
 
 def run_router(args, rank, world, local_rank):
@@ -985,10 +985,10 @@ def run_router(args, rank, world, local_rank):
             "data": "synthetic",
             "config": {"workload": f"router_T{T}_E{E}_k{k}_H{H}",
                        "l2": "256 MB written between timed calls (inputs fit in L2)"},
-            "roofline": {"bound": "hbm", "kernel": "router (5 launches)", "achieved": gbs, "peak": hbm_peak,
+            "roofline": {"bound": "hbm", "kernel": "router (3 launches: logits GEMM + top-k, scan, scatter)", "achieved": gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind, "traffic": None,
                          "algorithmic_bytes_per_launch": alg, "launch_ms": ms},
-            "gpu_launches": 5 * args.steps, "clocks": clk.summary()}), flush=True)
+            "gpu_launches": 3 * args.steps, "clocks": clk.summary()}), flush=True)
 
 
 def main():

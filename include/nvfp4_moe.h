@@ -184,8 +184,10 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
 /* ---------------------------------------------------------------------------
  * moe_router -- the router in front of moe_route_permute: the logits GEMM
  *   logits[t][e] = sum_h x[t][h] * w_gate[e][h]
- * on the tensor cores (bf16 inputs, FP32 sums), then moe_route_permute on
- * those logits.
+ * on the tensor cores (bf16 inputs, FP32 sums) with the top-k and softmax of
+ * every token in the same kernel, then the stable permutation of
+ * moe_route_permute (its selection rule and weights, bit for bit, on these
+ * logits).  Three kernels per call.
  *   "Tracing the Failure: Debugging CUTLASS FP4 Tile Configurations on
  *   Blackwell SM120", "The Broader Context" (each token scored against 256
  *   experts, 8 kept).  The pages give no gate formula: this is a bias-free
@@ -197,8 +199,9 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
  * Arguments (device pointers unless noted):
  *   x        bf16 [T][H] (raw bits), 16-byte aligned
  *   w_gate   bf16 [E][H], 16-byte aligned
- *   logits   f32 [T][E] out, or NULL (not written: the routing kernel adds
- *            the partial sums as it reads them)
+ *   logits   f32 [T][E] out, or NULL (not written: the partial sums are
+ *            added inside the router kernel and never leave the GPU's shared
+ *            memory)
  *   x_scale  f32 [1] out, or NULL: the NVFP4 decode multiplier of x,
  *            s = max|x| / (6*448) (1 when x is all zero), with max|x| taken
  *            by the logits GEMM from the x tiles it loads anyway -- what

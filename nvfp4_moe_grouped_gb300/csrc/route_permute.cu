@@ -21,14 +21,7 @@ namespace moe {
 namespace {
 
 constexpr int kRouteThreads = 256;      // scatter: one thread per (token, slot) item of a chunk
-constexpr int kTopkThreads = 1024;      // top-k: one warp per token of a chunk
-// Top-k from the router's partial sums when the chunks do not fill the GPU:
-// half the warps, two tokens each, so a thread may hold all of its token's
-// partial sums (kMaxSplits x 8 floats) and issue their loads at once instead
-// of in register-limited rounds (T = 1024: 42 -> 37 us per router call).  With
-// more chunks than SMs the full-width blocks are faster.
-constexpr int kPartsThreads = 512;
-constexpr int kMaxSplits = 8;           // the router splits K at most this many ways
+constexpr int kTopkThreads = 1024;      // top-k (a single-chunk layer): one warp per token
 
 struct RouteDims {
   int T, E, k, chunk_tokens, n_chunks;
@@ -43,33 +36,21 @@ inline RouteDims route_dims(int T, int E, int k) {
   return d;
 }
 
-// Logits given as FP32 partial sums over K ranges (the router's split GEMM):
-// logit[t][e] = sum over s, in order, of part[t / 128][s][t % 128][e].
-struct PartialLogits {
-  const float* part;  // [tiles][splits][128][NE]
-  int splits, NE;
-  float* logits_out;  // optional copy of the summed logits, [T][E]
-  const uint32_t* x_amax_bits;  // optional: max |x| as an f32 bit pattern ...
-  float* x_scale;               // ... turned into x's NVFP4 decode multiplier here
-};
-
 // Top-k and softmax of tokens [t0, t1), one warp per token (warps of the whole
 // block in turn); counts each selected expert in the shared histogram `hist`.
-// Plain logits (E <= 256): a warp loads its next token's row while it ranks
-// the current one.  BATCH (partial sums, NV <= 8, at most kMaxSplits splits): all loads
-// first.
-template <int NV, bool PARTS, bool BATCH = false>  // NV: logits per lane, NV * 32 >= E; PARTS: read partial sums
+// For E <= 256 a warp loads its next token's row while it ranks the current
+// one.
+template <int NV>  // logits per lane, NV * 32 >= E
 MOE_DEVINL void route_tokens(const float* __restrict__ logits, const RouteDims& d, int t0, int t1,
-                             int32_t* __restrict__ topk_id, float* __restrict__ topk_w, int* hist,
-                             const PartialLogits& pl) {
+                             int32_t* __restrict__ topk_id, float* __restrict__ topk_w, int* hist) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nw = blockDim.x / 32;
   uint32_t taken = 0;
 #pragma unroll
   for (int i = 0; i < NV; ++i)
     if (lane + 32 * i >= d.E) taken |= 1u << i;
-  constexpr bool kAhead = !PARTS && NV <= 8;
-  float nxt[NV];  // plain logits: the row of the warp's next token
+  constexpr bool kAhead = NV <= 8;
+  float nxt[NV];  // the row of the warp's next token
   if (kAhead) {
     const float* row = logits + static_cast<int64_t>(t0 + warp < t1 ? t0 + warp : t0) * d.E;
 #pragma unroll
@@ -77,50 +58,18 @@ MOE_DEVINL void route_tokens(const float* __restrict__ logits, const RouteDims& 
   }
   for (int t = t0 + warp; t < t1; t += nw) {
     float v[NV];
+    if (kAhead) {
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = kAhead ? nxt[i] : 0.0f;
-    if (!PARTS && !kAhead) {
+      for (int i = 0; i < NV; ++i) v[i] = nxt[i];
+      if (t + nw < t1) {
+        const float* row = logits + static_cast<int64_t>(t + nw) * d.E;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) nxt[i] = (taken >> i & 1u) ? 0.0f : __ldg(row + lane + 32 * i);
+      }
+    } else {
       const float* row = logits + static_cast<int64_t>(t) * d.E;
 #pragma unroll
       for (int i = 0; i < NV; ++i) v[i] = (taken >> i & 1u) ? 0.0f : __ldg(row + lane + 32 * i);
-    }
-    if (kAhead && t + nw < t1) {
-      const float* row = logits + static_cast<int64_t>(t + nw) * d.E;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) nxt[i] = (taken >> i & 1u) ? 0.0f : __ldg(row + lane + 32 * i);
-    }
-    if (PARTS && BATCH) {
-      // every partial sum of the lane's experts loaded at once, then added in split order
-      const float* src = pl.part + (static_cast<int64_t>(t >> 7) * pl.splits * 128 + (t & 127)) * pl.NE + lane;
-      float pv[kMaxSplits][NV];
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplits; ++sp)
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-          pv[sp][i] = (sp < pl.splits && lane + 32 * i < d.E) ? __ldg(src + static_cast<int64_t>(sp) * 128 * pl.NE + 32 * i)
-                                                              : 0.0f;
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplits; ++sp)
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-          if (sp < pl.splits && lane + 32 * i < d.E) v[i] = __fadd_rn(v[i], pv[sp][i]);
-    } else if (PARTS) {
-      // splits outermost, so each step issues the NV independent loads of all the lane's experts
-      const float* src = pl.part + (static_cast<int64_t>(t >> 7) * pl.splits * 128 + (t & 127)) * pl.NE + lane;
-#pragma unroll 8
-      for (int sp = 0; sp < pl.splits; ++sp) {
-        const float* s_row = src + static_cast<int64_t>(sp) * 128 * pl.NE;
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-          if (lane + 32 * i < d.E) v[i] = __fadd_rn(v[i], __ldg(s_row + 32 * i));
-      }
-    }
-    if (PARTS) {
-      if (pl.logits_out) {
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-          if (lane + 32 * i < d.E) pl.logits_out[static_cast<int64_t>(t) * d.E + lane + 32 * i] = v[i];
-      }
     }
     int my_i;
     float my_w;
@@ -134,30 +83,18 @@ MOE_DEVINL void route_tokens(const float* __restrict__ logits, const RouteDims& 
   }
 }
 
-// x's NVFP4 decode multiplier from the router GEMM's max |x| (block 0, thread 0).
-MOE_DEVINL void router_x_scale(const PartialLogits& pl) {
-  if (pl.x_scale && blockIdx.x == 0 && threadIdx.x == 0) {
-    const float a = __uint_as_float(*pl.x_amax_bits);
-    *pl.x_scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);  // s = amax / (6 * 448), 1 when amax = 0
-  }
-}
-
-template <int NV, bool PARTS, bool BATCH = false>
-__global__ void __launch_bounds__(PARTS ? (BATCH ? kPartsThreads : kTopkThreads) : kRouteThreads,
-                                  PARTS || NV > 8 ? 1 : 4)
-    route_kernel(const float* __restrict__ logits,
-                                                                                   RouteDims d,
-                                                              int32_t* __restrict__ topk_id,
-                                                              float* __restrict__ topk_w,
-                                                              int32_t* __restrict__ chunk_counts,
-                                                              PartialLogits pl) {
+template <int NV>
+__global__ void __launch_bounds__(kRouteThreads, NV > 8 ? 1 : 4) route_kernel(const float* __restrict__ logits,
+                                                                             RouteDims d,
+                                                                             int32_t* __restrict__ topk_id,
+                                                                             float* __restrict__ topk_w,
+                                                                             int32_t* __restrict__ chunk_counts) {
   extern __shared__ int hist[];  // [E]
-  if (PARTS) router_x_scale(pl);
   const int t0 = blockIdx.x * d.chunk_tokens;
   const int t1 = min(d.T, t0 + d.chunk_tokens);
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  route_tokens<NV, PARTS, BATCH>(logits, d, t0, t1, topk_id, topk_w, hist, pl);
+  route_tokens<NV>(logits, d, t0, t1, topk_id, topk_w, hist);
   __syncthreads();
   int32_t* out = chunk_counts + static_cast<int64_t>(blockIdx.x) * d.E;
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) out[e] = hist[e];
@@ -198,12 +135,26 @@ MOE_DEVINL int block_exclusive_scan(int v, int* warp_tot) {
 // chunk's row) and splits the chunks into 32 groups, one per warp; the group
 // sums are scanned per expert in shared memory, then every thread rewrites its
 // chunks from its group's base.  The expert offsets themselves (a scan over
-// experts) are left to the scatter.
+// experts) are left to the scatter.  With `amax_part` (n_parts max |x| words,
+// f32 bit patterns, from the router's CTAs), block 0's first warp also writes
+// x's NVFP4 decode multiplier s = amax / (6 * 448) (1 when amax = 0).
 __global__ void __launch_bounds__(1024) chunk_scan_kernel(RouteDims d, int32_t* __restrict__ chunk_counts,
-                                                          int32_t* __restrict__ expert_total) {
+                                                          int32_t* __restrict__ expert_total,
+                                                          const uint32_t* __restrict__ amax_part, int n_parts,
+                                                          float* __restrict__ x_scale) {
   __shared__ int part[32][33];  // [group][expert of the block], then each group's base
   constexpr int kB = 8;         // loads issued together
   const int g = threadIdx.x >> 5, c = threadIdx.x & 31;
+  if (amax_part && blockIdx.x == 0 && g == 0) {
+    uint32_t m = 0;
+    for (int i = c; i < n_parts; i += 32) m = max(m, amax_part[i]);  // non-negative patterns order as values
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (c == 0) {
+      const float a = __uint_as_float(m);
+      *x_scale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+    }
+  }
   const int e = blockIdx.x * 32 + c;
   const bool act = e < d.E;
   const int b0 = static_cast<int>(static_cast<int64_t>(g) * d.n_chunks / 32);
@@ -334,19 +285,18 @@ __global__ void __launch_bounds__(kRouteThreads) scatter_kernel(RouteDims d, con
 // chunk (T * k <= 256): top-k, expert offsets and the stable scatter, without
 // the scan and scatter launches (small decode batches are launch-bound).
 // 1024 threads, E <= 1024; dynamic shared memory 2 * E ints.
-template <int NV, bool PARTS>
+template <int NV>
 __global__ void __launch_bounds__(kTopkThreads) route_one_chunk_kernel(
     const float* __restrict__ logits, RouteDims d, int32_t* __restrict__ topk_id, float* __restrict__ topk_w,
     int32_t* __restrict__ expert_offsets, int32_t* __restrict__ pad_offsets, int32_t* __restrict__ perm_to_expanded,
-    int32_t* __restrict__ expanded_to_perm, int32_t* __restrict__ expanded_to_row, PartialLogits pl) {
+    int32_t* __restrict__ expanded_to_perm, int32_t* __restrict__ expanded_to_row) {
   extern __shared__ int sm[];
   int* hist = sm;        // [E] items per expert, then each expert's first position
   int* cnt = sm + d.E;   // [E] items of each expert placed so far
   __shared__ int warp_tot[32];
-  if (PARTS) router_x_scale(pl);
   for (int e = threadIdx.x; e < d.E; e += blockDim.x) { hist[e] = 0; cnt[e] = 0; }
   __syncthreads();
-  route_tokens<NV, PARTS>(logits, d, 0, d.T, topk_id, topk_w, hist, pl);
+  route_tokens<NV>(logits, d, 0, d.T, topk_id, topk_w, hist);
   __syncthreads();
   // expert offsets and padded (128-row) offsets: thread e holds expert e
   const int e = threadIdx.x;
@@ -416,29 +366,22 @@ int32_t* route_pad_offsets(void* ws, int T, int E, int k) {
 }  // namespace moe
 
 namespace moe {
-// Routing and permutation from full logits, or (part != nullptr) from the
-// router GEMM's partial sums.  Arguments are validated by the callers.
-moe_status route_permute_enqueue(const float* logits, const float* part, int splits, int NE, float* logits_out,
-                                 const uint32_t* x_amax_bits, float* x_scale, int T, int E, int k, int32_t* topk_id,
-                                 float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
-                                 int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws, cudaStream_t st) {
-  if (part && splits > kMaxSplits) return MOE_ERR_UNSUPPORTED;
+// Routing and permutation from full logits.  Arguments are validated by the
+// callers.
+moe_status route_permute_enqueue(const float* logits, int T, int E, int k, int32_t* topk_id, float* topk_w,
+                                 int32_t* expert_offsets, int32_t* perm_to_expanded, int32_t* expanded_to_perm,
+                                 int32_t* expanded_to_row, void* ws, cudaStream_t st) {
   RouteDims d = route_dims(T, E, k);
   int32_t* counts = static_cast<int32_t*>(ws);
   int32_t* pads = route_pad_offsets(ws, T, E, k);
   int32_t* totals = pads + ((static_cast<size_t>(E + 1) * sizeof(int32_t) + 255) / 256) * 256 / sizeof(int32_t);
   const size_t hist_bytes = sizeof(int) * E;
   const int nv = (E + 31) / 32;
-  const PartialLogits pl{part, splits, NE, logits_out, x_amax_bits, x_scale};
   if (d.n_chunks == 1) {
     const size_t one_bytes = 2 * sizeof(int) * E;
 #define MOE_ROUTE1(NV)                                                                                           \
-  (part ? route_one_chunk_kernel<NV, true><<<1, kTopkThreads, one_bytes, st>>>(                                  \
-              logits, d, topk_id, topk_w, expert_offsets, pads, perm_to_expanded, expanded_to_perm, expanded_to_row, \
-              pl)                                                                                                \
-        : route_one_chunk_kernel<NV, false><<<1, kTopkThreads, one_bytes, st>>>(                                 \
-              logits, d, topk_id, topk_w, expert_offsets, pads, perm_to_expanded, expanded_to_perm, expanded_to_row, \
-              pl))
+  route_one_chunk_kernel<NV><<<1, kTopkThreads, one_bytes, st>>>(logits, d, topk_id, topk_w, expert_offsets, pads, \
+                                                                 perm_to_expanded, expanded_to_perm, expanded_to_row)
     if (nv <= 1) MOE_ROUTE1(1);
     else if (nv <= 2) MOE_ROUTE1(2);
     else if (nv <= 4) MOE_ROUTE1(4);
@@ -448,13 +391,7 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
 #undef MOE_ROUTE1
     return check_launch();
   }
-  const bool batch = part != nullptr && d.n_chunks < num_sms();
-#define MOE_ROUTE(NV)                                                                                         \
-  (part ? (batch ? route_kernel<NV, true, NV <= 8><<<d.n_chunks, NV <= 8 ? kPartsThreads : kTopkThreads, hist_bytes,   \
-                                                    st>>>(logits, d, topk_id, topk_w, counts, pl)                      \
-                 : route_kernel<NV, true><<<d.n_chunks, kTopkThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w,    \
-                                                                                       counts, pl))                  \
-        : route_kernel<NV, false><<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts, pl))
+#define MOE_ROUTE(NV) route_kernel<NV><<<d.n_chunks, kRouteThreads, hist_bytes, st>>>(logits, d, topk_id, topk_w, counts)
   if (nv <= 1) MOE_ROUTE(1);
   else if (nv <= 2) MOE_ROUTE(2);
   else if (nv <= 4) MOE_ROUTE(4);
@@ -462,10 +399,35 @@ moe_status route_permute_enqueue(const float* logits, const float* part, int spl
   else if (nv <= 16) MOE_ROUTE(16);
   else MOE_ROUTE(32);
 #undef MOE_ROUTE
-  chunk_scan_kernel<<<(E + 31) / 32, 1024, 0, st>>>(d, counts, totals);
+  chunk_scan_kernel<<<(E + 31) / 32, 1024, 0, st>>>(d, counts, totals, nullptr, 0, nullptr);
   scatter_kernel<<<d.n_chunks, kRouteThreads, 3 * hist_bytes, st>>>(d, topk_id, counts, totals, expert_offsets, pads,
                                                                     perm_to_expanded, expanded_to_perm,
                                                                     expanded_to_row);
+  return check_launch();
+}
+}  // namespace moe
+
+namespace moe {
+// Scan and stable scatter of routing already in topk_id, whose per-chunk expert
+// counts (chunks of chunk_tokens tokens, chunk_tokens * k <= 256) are in
+// chunk_counts; the router's per-CTA amax words (optional) become x's decode
+// multiplier.  pad_offsets and expert_totals: E + 1 and E ints of scratch.
+moe_status route_scan_scatter_enqueue(int T, int E, int k, int chunk_tokens, const int32_t* topk_id,
+                                      int32_t* chunk_counts, int32_t* pad_offsets, int32_t* expert_totals,
+                                      const uint32_t* amax_part, int n_parts, float* x_scale,
+                                      int32_t* expert_offsets, int32_t* perm_to_expanded, int32_t* expanded_to_perm,
+                                      int32_t* expanded_to_row, cudaStream_t st) {
+  if (chunk_tokens < 1 || static_cast<int64_t>(chunk_tokens) * k > kRouteThreads) return MOE_ERR_INVALID_ARG;
+  RouteDims d;
+  d.T = T;
+  d.E = E;
+  d.k = k;
+  d.chunk_tokens = chunk_tokens;
+  d.n_chunks = (T + chunk_tokens - 1) / chunk_tokens;
+  chunk_scan_kernel<<<(E + 31) / 32, 1024, 0, st>>>(d, chunk_counts, expert_totals, amax_part, n_parts, x_scale);
+  scatter_kernel<<<d.n_chunks, kRouteThreads, 3 * sizeof(int) * E, st>>>(
+      d, topk_id, chunk_counts, expert_totals, expert_offsets, pad_offsets, perm_to_expanded, expanded_to_perm,
+      expanded_to_row);
   return check_launch();
 }
 }  // namespace moe
@@ -481,7 +443,7 @@ extern "C" moe_status moe_route_permute(const float* logits, int T, int E, int k
   if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(T) * k > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < moe_route_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
-  return route_permute_enqueue(logits, nullptr, 0, 0, nullptr, nullptr, nullptr, T, E, k, topk_id, topk_w,
+  return route_permute_enqueue(logits, T, E, k, topk_id, topk_w,
                                expert_offsets, perm_to_expanded, expanded_to_perm, expanded_to_row, ws,
                                static_cast<cudaStream_t>(stream));
 }

@@ -1,7 +1,7 @@
 // router.cu -- the router in front of the routing step: the logits GEMM
 //   logits[t][e] = sum_h x[t][h] * w_gate[e][h]      (bf16 inputs, FP32 sums)
-// on the 5th-generation tensor cores, then the top-k routing and stable
-// permutation of route_permute.cu on those logits.
+// on the 5th-generation tensor cores, with the top-k and softmax of every
+// token in the same kernel; then the stable permutation's scan and scatter.
 //
 // "Tracing the Failure: Debugging CUTLASS FP4 Tile Configurations on Blackwell
 // SM120", section "The Broader Context": every token is scored against the 256
@@ -10,66 +10,110 @@
 //
 // The contraction is small (T x E x H = 1024 x 256 x 6144 at decode) and its
 // inputs are read once, so the launch is spread over the GPU by splitting K:
-// CTA (tile, split) multiplies 128 tokens by all E (<= 256) experts over its
-// share of H with tcgen05.mma kind::f16 (M = 128 tokens, N = E rounded up to 16,
-// K = 16, FP32 accumulator in tensor memory) and stores its FP32 partial tile.
-// The routing kernel adds the partials in split order (deterministic) as it
-// reads each token's logits, so the logits never make a round trip of their
-// own.  Roles in the GEMM CTA: lane 0 of warp 0 issues the TMA loads (128-byte
-// swizzle, rows past T or E read as zeros), lane 0 of warp 1 the MMAs, warps 2
-// and 3 (when asked) take max |x| over the x tiles for the activation
-// quantiser, half of each stage each, two |bf16| patterns per 32-bit word
-// (one warp taking them one by one held the mainloop to its pace); all four
-// warps then drain the accumulator.  Every wait is bounded.
+// the S (<= 8) CTAs of a cluster share one tile of 128 tokens, CTA (tile,
+// split) multiplying the tile by all E (<= 256) experts over its share of H
+// with tcgen05.mma kind::f16 (M = 128 tokens, N = E rounded up to 16, K = 16,
+// FP32 accumulator in tensor memory).  The partial sums then never leave the
+// cluster: each CTA drains its accumulator and stores every token row into the
+// shared memory of the CTA that owns the token (128 / S tokens per CTA); each
+// owner adds its rows' S partial rows in split order (deterministic), and one
+// warp per token runs the top-k and softmax (k rounds of a warp max and a warp
+// min reduction), writing the routing and the counts of its chunk of (token,
+// slot) items; the scan and the stable scatter of route_permute.cu follow.
+// Roles: lane 0 of warp 0 issues the TMA loads (128-byte swizzle, rows past T
+// or E read as zeros), lane 0 of warp 1 the MMAs, warps 2 and 3 (when asked)
+// take max |x| over the x tiles for the activation quantiser (the scan kernel
+// combines the CTAs' words into x's decode multiplier); all eight warps drain
+// and route.  Every mbarrier wait is bounded; every CTA reaches both cluster
+// barriers on every path, and a CTA whose waits gave up marks the tile void in
+// its peers.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
-moe_status route_permute_enqueue(const float* logits, const float* part, int splits, int NE, float* logits_out,
-                                 const uint32_t* x_amax_bits, float* x_scale, int T, int E, int k, int32_t* topk_id,
-                                 float* topk_w, int32_t* expert_offsets, int32_t* perm_to_expanded,
-                                 int32_t* expanded_to_perm, int32_t* expanded_to_row, void* ws, cudaStream_t st);
+moe_status route_scan_scatter_enqueue(int T, int E, int k, int chunk_tokens, const int32_t* topk_id,
+                                      int32_t* chunk_counts, int32_t* pad_offsets, int32_t* expert_totals,
+                                      const uint32_t* amax_part, int n_parts, float* x_scale,
+                                      int32_t* expert_offsets, int32_t* perm_to_expanded, int32_t* expanded_to_perm,
+                                      int32_t* expanded_to_row, cudaStream_t st);
 namespace {
 
-constexpr int kRThreads = 128;
+constexpr int kRThreads = 256;
 constexpr int kRStages = 4;
 constexpr int kRBK = 64;                     // bf16 elements per K block (128 bytes of a row)
 constexpr int kRAStage = 128 * 128;          // 128 tokens x 128 bytes
 constexpr int kRBStage = 256 * 128;          // up to 256 experts x 128 bytes
-constexpr int kRSmem = kRStages * (kRAStage + kRBStage) + 128 + 1024;  // stages, barriers, alignment slack
+constexpr int kRStageArea = kRStages * (kRAStage + kRBStage);
+constexpr int kRMaxSplits = 8;               // a portable cluster size
+constexpr int kRAmaxWarps = 2;               // warps 2 and 3 take max |x|, half of each x stage each
+// after the MMAs the stage area holds the partial rows this CTA owns ([S][128 / S][NE] floats, 128 KB at
+// NE = 256), its chunk counts (at most 16 chunks x E ints: a chunk holds at least 8 tokens) and one void
+// flag per peer
+constexpr int kRRecvBytes = 128 * 256 * 4;
+constexpr int kRHistOff = kRRecvBytes;
+constexpr int kRHistBytes = 16 * 256 * 4;
+constexpr int kRFlagOff = kRHistOff + kRHistBytes;
+static_assert(kRFlagOff + 64 <= kRStageArea, "exchange area fits the stage area");
+constexpr int kRSmem = kRStageArea + 128 + 1024;  // stages, barriers, alignment slack
 constexpr uint32_t kRTmemCols = 256;
 
 struct RouterParams {
-  int T, E, NE, KB, splits;
-  float* part;           // [tiles][splits][128][NE]
-  uint32_t* amax_bits;   // optional: max |x| (bit pattern), for the activation quantiser
+  int T, E, NE, KB, k, group, chunk_tokens, n_chunks;
+  uint32_t* amax_part;   // optional: max |x| (bit pattern) of each amax warp's x tiles, [tiles * splits * 2]
+  float* logits;         // optional [T][E]
+  int32_t* topk_id;
+  float* topk_w;
+  int32_t* chunk_counts;  // [n_chunks][E]: items of each expert in each chunk of chunk_tokens tokens
   int32_t* err;
   uint64_t timeout_ns;
 };
 
+MOE_DEVINL void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+MOE_DEVINL void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// The partial logits a CTA owns sit column-major: [split][float4 chunk c of
+// the experts][token slot g], so a warp storing one chunk of 32 consecutive
+// token rows, and a thread reading its token's chunks in order, both touch
+// consecutive 16-byte words.
+MOE_DEVINL int recv_off(int split, int c, int g, int G, int nc4) { return ((split * nc4 + c) * G + g) * 4; }
+
+template <int NV>  // logits per lane: 32 NV >= E
 __global__ void __launch_bounds__(kRThreads, 1)
-    router_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+    router_topk_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                        const RouterParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_a = smem;
   uint8_t* s_b = smem + kRStages * kRAStage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_b + kRStages * kRBStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRStageArea);
   uint64_t* empty = full + kRStages;
   uint64_t* acc_full = empty + kRStages;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  float* s_recv = reinterpret_cast<float*>(smem);
+  int* s_hist = reinterpret_cast<int*>(smem + kRHistOff);
+  volatile int* s_void = reinterpret_cast<volatile int*>(smem + kRFlagOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, split = blockIdx.y;
-  const int kb0 = static_cast<int>(static_cast<int64_t>(split) * p.KB / p.splits);
-  const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.KB / p.splits);
+  const int tile = blockIdx.x, split = blockIdx.y, S = gridDim.y;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(split) * p.KB / S);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.KB / S);
   const int nk = kb1 - kb0;  // >= 1: splits <= KB
   const uint32_t b_bytes = static_cast<uint32_t>(p.NE) * 128;
 
-  const bool amax_on = p.amax_bits != nullptr;
+  const bool amax_on = p.amax_part != nullptr;
   if (threadIdx.x == 0) {
-    // a stage is free once the MMAs and (when x's amax is wanted) warps 2 and 3 are done with it
-    for (int s = 0; s < kRStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], amax_on ? 3 : 1); }
+    // a stage is free once the MMAs and (when x's amax is wanted) both amax warps are done with it
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], amax_on ? 1 + kRAmaxWarps : 1);
+    }
     mbar_init(acc_full, 1);
     *s_abort = 0;
     fence_barrier_init();
@@ -100,7 +144,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       tma_load_2d(s_b + s * kRBStage, &tm_w, &full[s], (kb0 + i) * kRBK, 0, pol);
       issued = i + 1;
     }
-    // let the copies this CTA started land before it can exit (the last kRStages fills)
+    // let the copies this CTA started land before the stage area is reused (the last kRStages fills)
     int zero = 0;
     for (int i = issued - kRStages > 0 ? issued - kRStages : 0; i < issued; ++i)
       mbar_wait_bounded(&full[i % kRStages], static_cast<uint32_t>(i / kRStages) & 1u, p.timeout_ns,
@@ -126,11 +170,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     mma_commit(acc_full);  // arrives once every MMA issued above has completed
   } else if ((warp == 2 || warp == 3) && amax_on) {
-    // ---- max |x| over this CTA's x tiles (each x element is in exactly one CTA's tiles; rows past T
-    // are zero-filled), for the NVFP4 decode multiplier of the activation quantiser: warp 2 the first
-    // half of every stage, warp 3 the second; |bf16| bit patterns order like the values ----
+    // ---- max |x| over this CTA's x tiles (each x element is in exactly one CTA's tiles; rows past T are
+    // zero-filled), for the NVFP4 decode multiplier of the activation quantiser: warp 2 the first half
+    // of every stage, warp 3 the second; |bf16| patterns order like the values, two per 32-bit word ----
     const int hw = warp - 2;
-    uint32_t m2 = 0;  // maxima of the two halfwords
+    uint32_t m2 = 0;  // per-halfword maxima
     for (int i = 0; i < nk; ++i) {
       const int s = i % kRStages;
       const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
@@ -157,30 +201,109 @@ __global__ void __launch_bounds__(kRThreads, 1)
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0 && m > 0) atomicMax(p.amax_bits, m << 16);  // the bf16 pattern as an f32 pattern
+    if (lane == 0) p.amax_part[(tile * S + split) * kRAmaxWarps + hw] = m << 16;  // as an f32 pattern
   }
   __syncwarp();
 
-  // ---- epilogue: all four warps; thread = token row of the tile (its TMEM lane) ----
+  // ---- epilogue: all eight warps ----
   const bool got = mbar_wait_bounded(acc_full, 0, p.timeout_ns, s_abort);
   const int bad = __syncthreads_or(!got || *s_abort);
+  if (threadIdx.x == 0 && !got && !*s_abort) record_error(p.err, MOE_ERR_TIMEOUT, 32);
   tc_fence_after();
+  // the stage area was last written by the tensor-memory copies (async proxy); order those writes before
+  // the generic stores made into it from here on (the void flags below, the peers' rows after the barrier)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (threadIdx.x < kRMaxSplits) s_void[threadIdx.x] = 0;  // peers write here only after the barrier
+  cluster_sync_all();  // every CTA of the tile is done with its stage area
+  const int G = p.group;
   if (!bad) {
-    const int r = warp * 32 + lane;
-    float* dst = p.part + (static_cast<int64_t>(tile * p.splits + split) * 128 + r) * p.NE;
-    for (int c0 = 0; c0 < p.NE; c0 += 32) {
+    // this CTA's partial row of token r (its TMEM lane) goes to owner r / G, slot [split][r % G]; warp w
+    // drains lane quadrant w % 4, the 32-column blocks 32 * (w / 4) + 64 j
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int nc4 = p.NE / 4;
+    const uint32_t base = map_shared_rank(smem_u32(s_recv), static_cast<uint32_t>(r / G));
+    for (int c0 = 32 * (warp >> 2); c0 < p.NE; c0 += 64) {
       uint32_t v[32];
-      tmem_ld_32cols(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+      tmem_ld_32cols(tmem + (static_cast<uint32_t>(q4 * 32) << 16) + c0, v);
       tmem_ld_wait();
-      const int cn = min(32, p.NE - c0);  // NE is a multiple of 16
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        if (j < cn)
-          *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                                 __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+      for (int i = 0; i < 8; ++i) {
+        const int c = (c0 >> 2) + i;
+        if (c < nc4)  // NE is a multiple of 16
+          st_cluster_v4(base + 4 * recv_off(split, c, r % G, G, nc4), v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                        v[4 * i + 3]);
+      }
     }
-  } else if (threadIdx.x == 0 && !got) {
-    record_error(p.err, MOE_ERR_TIMEOUT, 32);
+  } else if (threadIdx.x < S) {
+    // this tile's routing cannot be computed: say so to every CTA of the tile
+    st_cluster_u32(map_shared_rank(smem_u32(const_cast<int*>(s_void) + split), threadIdx.x), 1u);
+  }
+  cluster_sync_all();  // every partial row (or void flag) has landed
+  int void_any = 0;
+  for (int q = 0; q < S; ++q) void_any |= s_void[q];
+  // ---- the owner of tokens [tok0, tok0 + G): their S partial rows summed in split order into slot 0
+  // (and written out as logits when asked), then one thread per token: top-k, softmax, chunk counts.
+  // A void tile (its error already recorded) routes every token to experts 0..k-1 with weight 0, so that
+  // the scan and scatter after it stay within their buffers.
+  const int tok0 = tile * 128 + split * G;
+  const int CT = p.chunk_tokens;
+  const int n_cl = G / CT;  // chunks of this CTA's tokens
+  for (int i = threadIdx.x; i < n_cl * p.E; i += kRThreads) s_hist[i] = 0;
+  if (!void_any) {
+    const int nc4 = p.NE / 4;  // float4 chunks of a row
+    for (int i = threadIdx.x; i < G * nc4; i += kRThreads) {
+      const int c = i / G, g = i - c * G, e0 = 4 * c;
+      float4* dst = reinterpret_cast<float4*>(s_recv + recv_off(0, c, g, G, nc4));
+      float4 v = *dst;
+      for (int q = 1; q < S; ++q) {
+        const float4 u = *reinterpret_cast<const float4*>(s_recv + recv_off(q, c, g, G, nc4));
+        v.x = __fadd_rn(v.x, u.x);
+        v.y = __fadd_rn(v.y, u.y);
+        v.z = __fadd_rn(v.z, u.z);
+        v.w = __fadd_rn(v.w, u.w);
+      }
+      if (S > 1) *dst = v;
+      const int t = tok0 + g;
+      if (p.logits && t < p.T && e0 < p.E) {
+        float* lrow = p.logits + static_cast<int64_t>(t) * p.E + e0;
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j < p.E) lrow[j] = vv[j];
+      }
+    }
+  }
+  __syncthreads();
+  // one warp per token: its summed row from shared memory, the warp top-k and softmax, the routing out
+  // and its items counted in their chunk
+  const int nc4 = p.NE / 4;
+  for (int g = warp; g < G; g += kRThreads / 32) {
+    const int t = tok0 + g;
+    if (t >= p.T) break;  // the same for the whole warp
+    float v[NV];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = 0.0f;
+      if (e >= p.E) taken |= 1u << i;
+      else if (!void_any) v[i] = s_recv[recv_off(0, e >> 2, g, G, nc4) + (e & 3)];
+    }
+    int id = lane;
+    float w = 0.0f;
+    if (!void_any) warp_topk_softmax<NV>(v, taken, p.k, &id, &w);
+    if (lane < p.k) {
+      p.topk_id[static_cast<int64_t>(t) * p.k + lane] = id;
+      p.topk_w[static_cast<int64_t>(t) * p.k + lane] = w;
+      atomicAdd(&s_hist[(g / CT) * p.E + id], 1);
+    }
+  }
+  __syncthreads();
+  const int c_first = tok0 / CT;
+  for (int i = threadIdx.x; i < n_cl * p.E; i += kRThreads) {
+    const int c = c_first + i / p.E;
+    if (c < p.n_chunks) p.chunk_counts[static_cast<int64_t>(c) * p.E + i % p.E] = s_hist[i];
   }
   tc_fence_before();
   __syncthreads();
@@ -191,25 +314,56 @@ __global__ void __launch_bounds__(kRThreads, 1)
 }
 
 struct RouterShape {
-  int tiles, splits, NE, KB;
-  size_t part_bytes;
+  int tiles, splits, NE, KB, group, chunk_tokens, n_chunks;
 };
 
-RouterShape router_shape(int T, int E, int H) {
+int pow2_floor(int v) {
+  int r = 1;
+  while (2 * r <= v) r *= 2;
+  return r;
+}
+
+// Chunk of tokens whose items the scan counts together: a power of two that
+// divides the tokens a CTA routes (128 / splits) and keeps a chunk's items
+// within one scatter block (256).
+int router_chunk_tokens(int splits, int k) { return pow2_floor(std::min(128 / splits, std::max(1, 256 / k))); }
+
+// Splits: a power of two (a cluster of at most 8 CTAs per tile), so that the
+// tiles x splits CTAs fill the SMs, each with at least one K block.
+RouterShape router_shape(int T, int E, int H, int k) {
   RouterShape s;
   s.tiles = (T + 127) / 128;
   s.NE = (E + 15) / 16 * 16;
   s.KB = H / kRBK;
   const int sms = num_sms() > 0 ? num_sms() : 148;
-  // up to one CTA per SM, but at most 8 splits: each split adds T x E floats of partial sums that the
-  // routing kernel reads back per token
-  int splits = (sms + s.tiles - 1) / s.tiles;
-  if (splits > s.KB) splits = s.KB;
-  if (splits > 8) splits = 8;
-  if (splits < 1) splits = 1;
+  int splits = pow2_floor(std::max(1, sms / s.tiles));
+  splits = std::min(splits, std::min(kRMaxSplits, pow2_floor(s.KB)));
   s.splits = splits;
-  s.part_bytes = (static_cast<size_t>(s.tiles) * splits * 128 * s.NE * sizeof(float) + 255) / 256 * 256;
+  s.group = 128 / splits;
+  s.chunk_tokens = router_chunk_tokens(splits, k);
+  s.n_chunks = (T + s.chunk_tokens - 1) / s.chunk_tokens;
   return s;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace: per-CTA amax words, then the chunk counts, the padded offsets and
+// each expert's total; sized for the most CTAs and the most chunks any split
+// count gives.
+struct RouterWs {
+  size_t amax_off, counts_off, pads_off, totals_off, total;
+};
+RouterWs router_ws(int T, int E, int k) {
+  RouterWs w;
+  const int tiles = (T + 127) / 128;
+  const int ct_min = router_chunk_tokens(kRMaxSplits, k);
+  const int64_t chunks_max = (T + ct_min - 1) / ct_min;
+  w.amax_off = 0;
+  w.counts_off = align256(static_cast<size_t>(tiles) * kRMaxSplits * kRAmaxWarps * sizeof(uint32_t));
+  w.pads_off = w.counts_off + align256(static_cast<size_t>(chunks_max) * E * sizeof(int32_t));
+  w.totals_off = w.pads_off + align256(static_cast<size_t>(E + 1) * sizeof(int32_t));
+  w.total = w.totals_off + align256(static_cast<size_t>(E) * sizeof(int32_t));
+  return w;
 }
 
 // 2D bf16 map over [rows][cols], boxes of 64 columns (128 bytes) x box_rows, 128-byte swizzle.
@@ -225,6 +379,28 @@ bool make_bf16_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t co
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int NV>
+moe_status launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterParams& p, int tiles,
+                         int splits, cudaStream_t st) {
+  auto kern = router_topk_kernel<NV>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem) != cudaSuccess)
+    return MOE_ERR_RESOURCE;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(tiles, splits, 1);
+  cfg.blockDim = dim3(kRThreads, 1, 1);
+  cfg.dynamicSmemBytes = kRSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the splits of one tile form a cluster
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tm_x, tm_w, p) != cudaSuccess) return MOE_ERR_CUDA;
+  return check_launch();
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -232,8 +408,7 @@ using namespace moe;
 
 extern "C" size_t moe_router_workspace_size(int T, int E, int H, int k) {
   if (T < 1 || E < 1 || H < kRBK || k < 1) return 0;
-  const RouterShape s = router_shape(T, E, H);
-  return s.part_bytes + 256 + moe_route_permute_workspace_size(T, E, k);  // 256: the amax word
+  return router_ws(T, E, k).total;
 }
 
 extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int T, int E, int H, int k,
@@ -248,20 +423,28 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   if (static_cast<int64_t>(T) * k > 0x7FFFFFFF || static_cast<int64_t>(T) * E > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w_gate) || !aligned16(ws) || (logits && !aligned16(logits))) return MOE_ERR_MISALIGNED;
   if (!ws || ws_bytes < moe_router_workspace_size(T, E, H, k)) return MOE_ERR_WORKSPACE;
-  const RouterShape s = router_shape(T, E, H);
+  const RouterShape s = router_shape(T, E, H, k);
+  const RouterWs L = router_ws(T, E, k);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  float* part = reinterpret_cast<float*>(w8);
-  uint32_t* amax_bits = reinterpret_cast<uint32_t*>(w8 + s.part_bytes);
-  void* route_ws = w8 + s.part_bytes + 256;
+  uint32_t* amax_part = reinterpret_cast<uint32_t*>(w8 + L.amax_off);
+  int32_t* counts = reinterpret_cast<int32_t*>(w8 + L.counts_off);
+  int32_t* pads = reinterpret_cast<int32_t*>(w8 + L.pads_off);
+  int32_t* totals = reinterpret_cast<int32_t*>(w8 + L.totals_off);
 
   RouterParams p{};
   p.T = T;
   p.E = E;
   p.NE = s.NE;
   p.KB = s.KB;
-  p.splits = s.splits;
-  p.part = part;
-  p.amax_bits = x_scale ? amax_bits : nullptr;
+  p.k = k;
+  p.group = s.group;
+  p.chunk_tokens = s.chunk_tokens;
+  p.n_chunks = s.n_chunks;
+  p.amax_part = x_scale ? amax_part : nullptr;
+  p.logits = logits;
+  p.topk_id = topk_id;
+  p.topk_w = topk_w;
+  p.chunk_counts = counts;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
   if (!p.err) return MOE_ERR_CUDA;
@@ -269,15 +452,16 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   if (!make_bf16_map(&tm_x, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H), 128)) return MOE_ERR_CUDA;
   if (!make_bf16_map(&tm_w, w_gate, static_cast<uint64_t>(E), static_cast<uint64_t>(H), static_cast<uint32_t>(s.NE)))
     return MOE_ERR_CUDA;
-  if (cudaFuncSetAttribute(router_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem) != cudaSuccess)
-    return MOE_ERR_RESOURCE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (x_scale && cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-  router_gemm_kernel<<<dim3(s.tiles, s.splits), kRThreads, kRSmem, st>>>(tm_x, tm_w, p);
-  moe_status rs = check_launch();
+  const int nv = (s.NE + 31) / 32;
+  moe_status rs = nv <= 1   ? launch_router<1>(tm_x, tm_w, p, s.tiles, s.splits, st)
+                  : nv <= 2 ? launch_router<2>(tm_x, tm_w, p, s.tiles, s.splits, st)
+                  : nv <= 4 ? launch_router<4>(tm_x, tm_w, p, s.tiles, s.splits, st)
+                            : launch_router<8>(tm_x, tm_w, p, s.tiles, s.splits, st);
   if (rs != MOE_OK) return rs;
-  // the routing kernel adds the partial sums (in split order) as it reads each token's logits
-  return route_permute_enqueue(nullptr, part, s.splits, s.NE, logits, x_scale ? amax_bits : nullptr, x_scale, T, E,
-                               k, topk_id, topk_w, expert_offsets, perm_to_expanded, expanded_to_perm,
-                               expanded_to_row, route_ws, st);
+  // expert offsets, padded offsets and the stable scatter from the routing kernel's chunk counts; x's
+  // decode multiplier from the CTAs' amax words
+  return route_scan_scatter_enqueue(T, E, k, s.chunk_tokens, topk_id, counts, pads, totals,
+                                    x_scale ? amax_part : nullptr, s.tiles * s.splits * kRAmaxWarps, x_scale,
+                                    expert_offsets, perm_to_expanded, expanded_to_perm, expanded_to_row, st);
 }

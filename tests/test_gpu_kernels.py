@@ -207,8 +207,8 @@ def test_finalize_matches_oracle(T, k, N):
 
 # ------------------------------------------------------------------ router (logits GEMM + routing)
 
-# T*k <= 256: one routing kernel; up to 1024 tokens: fewer chunks than SMs (half-width blocks that load all
-# partial sums at once); 6144 tokens: 192 chunks, full-width blocks
+# the router kernel's K splits per 128-token tile (a cluster of that many CTAs): 4 (16 tokens, H = 256), 8 (129,
+# 300 and 1024 tokens), 2 (6144 tokens: 48 tiles); E = 40 leaves a partial 32-expert lane group
 @pytest.mark.parametrize("T,E,k,H", [(16, 8, 2, 256), (129, 40, 4, 512), (300, 256, 8, 1024), (1024, 256, 8, 6144),
                                      (6144, 256, 8, 512)])
 def test_router_matches_oracle(T, E, k, H):
