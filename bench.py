@@ -776,6 +776,28 @@ def run_gemm(args, rank, world, local_rank):
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 
+def cublaslt_reference(M, N, K, iters, peak_tflops):
+    """The same dense FP4 GEMM through cuBLASLt's block-scaled e2m1 matmul (a library timing reference built
+    beside the layer's library; operands hold a fixed pattern, only the time is used)."""
+    import ctypes
+    from nvfp4_moe_grouped_gb300 import build as nb
+    if not os.path.exists(nb.REF_LIB):
+        return {"status": "reference library not built"}
+    lib = ctypes.CDLL(nb.REF_LIB)
+    fn = lib.nvfp4_cublaslt_gemm_time
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_float), ctypes.c_char_p, ctypes.c_int]
+    ms = ctypes.c_float(0.0)
+    msg = ctypes.create_string_buffer(256)
+    rc = fn(M, N, K, 3, iters, ctypes.byref(ms), msg, 256)
+    if rc != 0:
+        return {"status": msg.value.decode(errors="replace")}
+    tf = 2.0 * M * N * K / (ms.value / 1e3) / 1e12
+    return {"library": "cuBLASLt block-scaled e2m1 x e2m1 (VEC16_UE4M3 scales), FP32 accumulate, bf16 out",
+            "ms": ms.value, "tflops": tf, "frac_of_fp4_peak": tf / peak_tflops, "status": "ok",
+            "timing": f"{iters} back-to-back calls after 3 warm-up calls, CUDA events"}
+
+
 def run_dense(args, rank, world, local_rank):
     """One dense NVFP4 GEMM, M = N = K = --dense-size (a 'very large matrices' measurement), BF16 out,
     against this GPU's measured dense FP4 MMA rate."""
@@ -829,6 +851,9 @@ def run_dense(args, rank, world, local_rank):
     fp4 = fp4_peaks(local_rank) if rank == 0 else None
     if rank == 0:
         peak_fp4 = fp4["peak_tflops"]
+        del codes, sf, pw, out
+        torch.cuda.empty_cache()
+        ref = cublaslt_reference(M, N, K, max(3, args.steps), peak_fp4)
         print(json.dumps({
             "metric": "dense NVFP4 GEMM TFLOPS vs dense FP4 peak", "value": tf, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -841,7 +866,7 @@ def run_dense(args, rank, world, local_rank):
                          "peak": peak_fp4, "unit": "TFLOP/s", "frac": tf / peak_fp4,
                          "peak_kind": FP4_PEAK_KIND,
                          "traffic": None, "algorithmic_flops_per_launch": flops, "launch_ms": ms},
-            "fp4_mma_probes": fp4,
+            "fp4_mma_probes": fp4, "cublaslt_reference": ref,
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 

@@ -18,6 +18,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libnvfp4_moe.so")
+# cuBLASLt's block-scaled FP4 GEMM as a timing reference for the dense GEMM (benchmark only)
+REF_SRC = os.path.join(HERE, "reference_gemm", "cublaslt_fp4.cu")
+REF_LIB = os.path.join(BUILD, "libnvfp4_cublaslt.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -71,7 +74,23 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
     os.replace(tmp, LIB)
+    build_reference()
     return LIB
+
+
+def build_reference() -> str | None:
+    """The cuBLASLt timing reference, a separate library (it links cuBLASLt dynamically; the layer's library
+    depends on the driver only).  A failure here is reported, not raised: nothing but the benchmark's dense-GEMM
+    comparison uses it."""
+    os.makedirs(BUILD, exist_ok=True)
+    tmp = REF_LIB + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-shared", REF_SRC, "-o", tmp, "-lcublasLt"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        print(f"note: the cuBLASLt reference library did not build:\n{res.stderr[-2000:]}")
+        return None
+    os.replace(tmp, REF_LIB)
+    return REF_LIB
 
 
 if __name__ == "__main__":

@@ -170,3 +170,17 @@ def test_finalize_and_forward_reject_before_launch(L):
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 200, 128, 1.0, P, P, 1 << 30, None) == UNSUPPORTED
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 256, 128, 0.0, P, P, 1 << 30, None) == INVALID
     assert L.moe_forward(P, P, ctypes.byref(w), 4, 8, 2, 256, 128, 1.0, P, P, 16, None) == WORKSPACE
+
+
+def test_cublaslt_reference_library_builds_and_exports():
+    """The dense-GEMM timing reference (cuBLASLt, benchmark only) is a separate library beside the layer's; it
+    builds with the package and exports its one entry point.  No GPU call is made."""
+    import ctypes
+    import os
+
+    from nvfp4_moe_grouped_gb300 import build as nb
+    path = nb.build_reference()
+    if path is None:
+        pytest.skip("cuBLASLt is not available to link against here")
+    assert os.path.exists(path) and path != nb.LIB
+    assert hasattr(ctypes.CDLL(path), "nvfp4_cublaslt_gemm_time")
