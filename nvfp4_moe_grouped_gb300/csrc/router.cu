@@ -10,7 +10,7 @@
 //
 // The contraction is small (T x E x H = 1024 x 256 x 6144 at decode) and its
 // inputs are read once, so the launch is spread over the GPU by splitting K:
-// the S (<= 8) CTAs of a cluster share one tile of 128 tokens, CTA (tile,
+// the S (<= 16) CTAs of a cluster share one tile of 128 tokens, CTA (tile,
 // split) multiplying the tile by all E (<= 256) experts over its share of H
 // with tcgen05.mma kind::f16 (M = 128 tokens, N = E rounded up to 16, K = 16,
 // FP32 accumulator in tensor memory).  The partial sums then never leave the
@@ -23,10 +23,11 @@
 // Roles: lane 0 of warp 0 issues the TMA loads (128-byte swizzle, rows past T
 // or E read as zeros), lane 0 of warp 1 the MMAs, warps 2 and 3 (when asked)
 // take max |x| over the x tiles for the activation quantiser (the scan kernel
-// combines the CTAs' words into x's decode multiplier); all eight warps drain
-// and route.  Every mbarrier wait is bounded; every CTA reaches both cluster
-// barriers on every path, and a CTA whose waits gave up marks the tile void in
-// its peers.
+// combines the CTAs' words into x's decode multiplier); all sixteen warps
+// drain and route (the phases after the MMAs are latency-bound, so more warps
+// shorten them).  Every mbarrier wait is bounded; every CTA reaches both
+// cluster barriers on every path, and a CTA whose waits gave up marks the tile
+// void in its peers.
 #include <algorithm>
 
 #include "common.cuh"
@@ -39,17 +40,17 @@ moe_status route_scan_scatter_enqueue(int T, int E, int k, int chunk_tokens, con
                                       int32_t* expanded_to_row, cudaStream_t st);
 namespace {
 
-constexpr int kRThreads = 256;
+constexpr int kRThreads = 512;
 constexpr int kRStages = 4;
 constexpr int kRBK = 64;                     // bf16 elements per K block (128 bytes of a row)
 constexpr int kRAStage = 128 * 128;          // 128 tokens x 128 bytes
 constexpr int kRBStage = 256 * 128;          // up to 256 experts x 128 bytes
 constexpr int kRStageArea = kRStages * (kRAStage + kRBStage);
-constexpr int kRMaxSplits = 8;               // a portable cluster size
+constexpr int kRMaxSplits = 16;              // 16 only where the device places clusters that large
 constexpr int kRAmaxWarps = 2;               // warps 2 and 3 take max |x|, half of each x stage each
 // after the MMAs the stage area holds the partial rows this CTA owns ([S][128 / S][NE] floats, 128 KB at
 // NE = 256), its chunk counts (at most 16 chunks x E ints: a chunk holds at least 8 tokens) and one void
-// flag per peer
+// flag per peer (at most 16)
 constexpr int kRRecvBytes = 128 * 256 * 4;
 constexpr int kRHistOff = kRRecvBytes;
 constexpr int kRHistBytes = 16 * 256 * 4;
@@ -57,6 +58,8 @@ constexpr int kRFlagOff = kRHistOff + kRHistBytes;
 static_assert(kRFlagOff + 64 <= kRStageArea, "exchange area fits the stage area");
 constexpr int kRSmem = kRStageArea + 128 + 1024;  // stages, barriers, alignment slack
 constexpr uint32_t kRTmemCols = 256;
+constexpr int kRDrainStep = 32 * (kRThreads / 128);  // columns between a drain warp's two 32-column blocks
+static_assert(2 * kRDrainStep >= static_cast<int>(kRTmemCols), "two blocks per drain warp cover the accumulator");
 
 struct RouterParams {
   int T, E, NE, KB, k, group, chunk_tokens, n_chunks;
@@ -218,21 +221,27 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int G = p.group;
   if (!bad) {
     // this CTA's partial row of token r (its TMEM lane) goes to owner r / G, slot [split][r % G]; warp w
-    // drains lane quadrant w % 4, the 32-column blocks 32 * (w / 4) + 64 j
+    // drains lane quadrant w % 4, the 32-column blocks 32 * (w / 4) and 32 * (w / 4) + 128, both loads in
+    // flight before one wait
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int nc4 = p.NE / 4;
     const uint32_t base = map_shared_rank(smem_u32(s_recv), static_cast<uint32_t>(r / G));
-    for (int c0 = 32 * (warp >> 2); c0 < p.NE; c0 += 64) {
-      uint32_t v[32];
-      tmem_ld_32cols(tmem + (static_cast<uint32_t>(q4 * 32) << 16) + c0, v);
-      tmem_ld_wait();
+    const uint32_t lane_cols = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const int c0 = 32 * (warp >> 2);
+    uint32_t v[2][32];
+    if (c0 < p.NE) tmem_ld_32cols(lane_cols + c0, v[0]);
+    if (c0 + kRDrainStep < p.NE) tmem_ld_32cols(lane_cols + c0 + kRDrainStep, v[1]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cb = c0 + h * kRDrainStep;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int c = (c0 >> 2) + i;
-        if (c < nc4)  // NE is a multiple of 16
-          st_cluster_v4(base + 4 * recv_off(split, c, r % G, G, nc4), v[4 * i], v[4 * i + 1], v[4 * i + 2],
-                        v[4 * i + 3]);
+        const int c = (cb >> 2) + i;
+        if (cb < p.NE && c < nc4)  // NE is a multiple of 16
+          st_cluster_v4(base + 4 * recv_off(split, c, r % G, G, nc4), v[h][4 * i], v[h][4 * i + 1],
+                        v[h][4 * i + 2], v[h][4 * i + 3]);
       }
     }
   } else if (threadIdx.x < S) {
@@ -243,14 +252,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
   int void_any = 0;
   for (int q = 0; q < S; ++q) void_any |= s_void[q];
   // ---- the owner of tokens [tok0, tok0 + G): their S partial rows summed in split order into slot 0
-  // (and written out as logits when asked), then one thread per token: top-k, softmax, chunk counts.
+  // (and written out as logits when asked), then one warp per token: top-k, softmax, chunk counts.
   // A void tile (its error already recorded) routes every token to experts 0..k-1 with weight 0, so that
   // the scan and scatter after it stay within their buffers.
   const int tok0 = tile * 128 + split * G;
   const int CT = p.chunk_tokens;
   const int n_cl = G / CT;  // chunks of this CTA's tokens
   for (int i = threadIdx.x; i < n_cl * p.E; i += kRThreads) s_hist[i] = 0;
-  if (!void_any) {
+  if (!void_any && (S > 1 || p.logits)) {  // one split and no logits wanted: slot 0 holds the sums already
     const int nc4 = p.NE / 4;  // float4 chunks of a row
     for (int i = threadIdx.x; i < G * nc4; i += kRThreads) {
       const int c = i / G, g = i - c * G, e0 = 4 * c;
@@ -275,9 +284,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   }
   __syncthreads();
+  const int nc4 = p.NE / 4;
   // one warp per token: its summed row from shared memory, the warp top-k and softmax, the routing out
   // and its items counted in their chunk
-  const int nc4 = p.NE / 4;
   for (int g = warp; g < G; g += kRThreads / 32) {
     const int t = tok0 + g;
     if (t >= p.T) break;  // the same for the whole warp
@@ -328,8 +337,55 @@ int pow2_floor(int v) {
 // within one scatter block (256).
 int router_chunk_tokens(int splits, int k) { return pow2_floor(std::min(128 / splits, std::max(1, 256 / k))); }
 
-// Splits: a power of two (a cluster of at most 8 CTAs per tile), so that the
-// tiles x splits CTAs fill the SMs, each with at least one K block.
+// Clusters of 16 CTAs of one router kernel variant that the current device
+// holds at once (0 where it refuses the non-portable size).
+template <int NV>
+int router_clusters16_of() {
+  auto kern = router_topk_kernel<NV>;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1, 16, 1);
+    cfg.blockDim = dim3(kRThreads, 1, 1);
+    cfg.dynamicSmemBytes = kRSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 16;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refusal above is an answer, not an error of a later launch
+  return n;
+}
+
+int router_nv_index(int NE) {
+  const int nv = (NE + 31) / 32;
+  return nv <= 1 ? 0 : nv <= 2 ? 1 : nv <= 4 ? 2 : 3;
+}
+
+// Looked up once per device and variant.
+int router_clusters16(int NE) {
+  static int cached[64][4] = {};  // clusters + 1; 0 = not looked up
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int i = router_nv_index(NE);
+  if (cached[dev][i] == 0) {
+    const int n = i == 0 ? router_clusters16_of<1>()
+                  : i == 1 ? router_clusters16_of<2>()
+                  : i == 2 ? router_clusters16_of<4>()
+                           : router_clusters16_of<8>();
+    cached[dev][i] = n + 1;
+  }
+  return cached[dev][i] - 1;
+}
+
+// Splits: a power of two, so that the tiles x splits CTAs fill the SMs, each
+// with at least one K block; 16 (a non-portable cluster) only where the device
+// holds every tile's cluster at once, else at most 8.
 RouterShape router_shape(int T, int E, int H, int k) {
   RouterShape s;
   s.tiles = (T + 127) / 128;
@@ -338,6 +394,7 @@ RouterShape router_shape(int T, int E, int H, int k) {
   const int sms = num_sms() > 0 ? num_sms() : 148;
   int splits = pow2_floor(std::max(1, sms / s.tiles));
   splits = std::min(splits, std::min(kRMaxSplits, pow2_floor(s.KB)));
+  if (splits > 8 && router_clusters16(s.NE) < s.tiles) splits = 8;
   s.splits = splits;
   s.group = 128 / splits;
   s.chunk_tokens = router_chunk_tokens(splits, k);
@@ -384,6 +441,8 @@ moe_status launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const
                          int splits, cudaStream_t st) {
   auto kern = router_topk_kernel<NV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem) != cudaSuccess)
+    return MOE_ERR_RESOURCE;
+  if (splits > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return MOE_ERR_RESOURCE;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(tiles, splits, 1);
