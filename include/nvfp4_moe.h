@@ -112,8 +112,8 @@ MOE_API moe_status moe_device_error(int32_t* code, int32_t* where);
 MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
 
 /* Test hooks: bit 0 makes the next grouped-GEMM launches skip filling their
- * first pipeline stage, so the bounded-wait path can be exercised without
- * faulting anything; bit 1 makes them keep the one-CTA 128-row tile where
+ * first pipeline stage (and moe_router's first CTA skip its first), so the
+ * bounded-wait path can be exercised without faulting anything; bit 1 makes them keep the one-CTA 128-row tile where
  * the CTA-pair tile would run, so both kernels can be compared on one input;
  * bit 2 makes moe_forward (and its graph) use the staged kernels for layers
  * the single-launch path would take.  0 (the default) for normal operation. */

@@ -33,6 +33,7 @@
 #include "common.cuh"
 
 namespace moe {
+int& gemm_debug_flags();
 moe_status route_scan_scatter_enqueue(int T, int E, int k, int chunk_tokens, const int32_t* topk_id,
                                       int32_t* chunk_counts, int32_t* pad_offsets, int32_t* expert_totals,
                                       const uint32_t* amax_part, int n_parts, float* x_scale,
@@ -70,6 +71,7 @@ struct RouterParams {
   int32_t* chunk_counts;  // [n_chunks][E]: items of each expert in each chunk of chunk_tokens tokens
   int32_t* err;
   uint64_t timeout_ns;
+  int debug_flags;  // bit 0: CTA (0, 0) never fills its first stage (bounded-wait test hook)
 };
 
 MOE_DEVINL void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     // ---- producer ----
     const uint64_t pol = l2_policy_evict_first();
     int issued = 0;
+    const bool skip_first = (p.debug_flags & 1) != 0 && tile == 0 && split == 0;
     for (int i = 0; i < nk; ++i) {
       const int s = i % kRStages;
       const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
@@ -142,6 +145,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         *s_abort = 1;
         break;
       }
+      if (i == 0 && skip_first) continue;  // stage 0 never fills: the MMA thread's wait gives up
       mbar_arrive_expect_tx(&full[s], kRAStage + b_bytes);
       tma_load_2d(s_a + s * kRAStage, &tm_x, &full[s], (kb0 + i) * kRBK, tile * 128, pol);
       tma_load_2d(s_b + s * kRBStage, &tm_w, &full[s], (kb0 + i) * kRBK, 0, pol);
@@ -506,6 +510,7 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   p.chunk_counts = counts;
   p.err = device_error_word();
   p.timeout_ns = wait_timeout_ns();
+  p.debug_flags = gemm_debug_flags();
   if (!p.err) return MOE_ERR_CUDA;
   CUtensorMap tm_x, tm_w;
   if (!make_bf16_map(&tm_x, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H), 128)) return MOE_ERR_CUDA;

@@ -245,6 +245,40 @@ def test_router_matches_oracle(T, E, k, H):
         assert srt[k - 1] - srt[k] <= 2 * bound[t].max(), t
 
 
+def test_router_timeout_path_reports_and_recovers():
+    """The router's first CTA never fills its first stage: its bounded waits give up, the launch reports
+    MOE_ERR_TIMEOUT, and that CTA's tile is void in every CTA of its cluster, so the tile's tokens go to
+    experts 0..k-1 with weight 0 (a valid routing the scan and scatter place). The other tiles route as a
+    clean call does, and the next call is exact."""
+    T, E, k, H = 300, 64, 4, 1024
+    x = inputs.activations(T, H, seed=T)
+    wg = inputs.router_gate(E, H)
+    xd, wgd = x.to(DEV), wg.to(DEV)
+    got = {}
+
+    def launch():
+        got["r"], _ = moe.moe_router(xd, wgd, k)
+        torch.cuda.synchronize()
+    code, _ = _run_with_timeout_hook(launch)
+    assert code == 6  # MOE_ERR_TIMEOUT
+    rv = got["r"]
+    ids_v, w_v = rv.topk_id.cpu().numpy(), rv.topk_w.cpu().numpy()
+    r, lg = moe.moe_router(xd, wgd, k)
+    torch.cuda.synchronize()
+    assert moe.device_error() == (0, 0)
+    ids, w = oracle.route(lg.cpu().numpy(), k)
+    assert np.array_equal(r.topk_id.cpu().numpy(), ids)
+    assert np.array_equal(r.topk_w.cpu().numpy().view(np.uint32), w.view(np.uint32))
+    assert np.array_equal(ids_v[:128], np.tile(np.arange(k), (128, 1)))
+    assert not w_v[:128].any()
+    assert np.array_equal(ids_v[128:], ids[128:])
+    assert np.array_equal(w_v[128:].view(np.uint32), w[128:].view(np.uint32))
+    offs, p2e, e2p = oracle.permute(ids_v, E)
+    assert np.array_equal(rv.expert_offsets.cpu().numpy(), offs)
+    assert np.array_equal(rv.perm_to_expanded.cpu().numpy(), p2e)
+    assert np.array_equal(rv.expanded_to_perm.cpu().numpy(), e2p)
+
+
 # ------------------------------------------------------------------ grouped GEMM
 
 def _routed_operand(x_bf16, offs):
