@@ -371,13 +371,19 @@ int router_nv_index(int NE) {
   return nv <= 1 ? 0 : nv <= 2 ? 1 : nv <= 4 ? 2 : 3;
 }
 
-// Looked up once per device and variant.
-int router_clusters16(int NE) {
+// Looked up once per device and variant, never while `st` is being captured
+// into a graph (a call made then takes 8-CTA clusters and looks up later).
+int router_clusters16(int NE, cudaStream_t st) {
   static int cached[64][4] = {};  // clusters + 1; 0 = not looked up
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int i = router_nv_index(NE);
   if (cached[dev][i] == 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+      cudaGetLastError();
+      return 0;
+    }
     const int n = i == 0 ? router_clusters16_of<1>()
                   : i == 1 ? router_clusters16_of<2>()
                   : i == 2 ? router_clusters16_of<4>()
@@ -390,7 +396,7 @@ int router_clusters16(int NE) {
 // Splits: a power of two, so that the tiles x splits CTAs fill the SMs, each
 // with at least one K block; 16 (a non-portable cluster) only where the device
 // holds every tile's cluster at once, else at most 8.
-RouterShape router_shape(int T, int E, int H, int k) {
+RouterShape router_shape(int T, int E, int H, int k, cudaStream_t st) {
   RouterShape s;
   s.tiles = (T + 127) / 128;
   s.NE = (E + 15) / 16 * 16;
@@ -398,7 +404,7 @@ RouterShape router_shape(int T, int E, int H, int k) {
   const int sms = num_sms() > 0 ? num_sms() : 148;
   int splits = pow2_floor(std::max(1, sms / s.tiles));
   splits = std::min(splits, std::min(kRMaxSplits, pow2_floor(s.KB)));
-  if (splits > 8 && router_clusters16(s.NE) < s.tiles) splits = 8;
+  if (splits > 8 && router_clusters16(s.NE, st) < s.tiles) splits = 8;
   s.splits = splits;
   s.group = 128 / splits;
   s.chunk_tokens = router_chunk_tokens(splits, k);
@@ -486,7 +492,8 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   if (static_cast<int64_t>(T) * k > 0x7FFFFFFF || static_cast<int64_t>(T) * E > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w_gate) || !aligned16(ws) || (logits && !aligned16(logits))) return MOE_ERR_MISALIGNED;
   if (!ws || ws_bytes < moe_router_workspace_size(T, E, H, k)) return MOE_ERR_WORKSPACE;
-  const RouterShape s = router_shape(T, E, H, k);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const RouterShape s = router_shape(T, E, H, k, st);
   const RouterWs L = router_ws(T, E, k);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   uint32_t* amax_part = reinterpret_cast<uint32_t*>(w8 + L.amax_off);
@@ -516,7 +523,6 @@ extern "C" moe_status moe_router(const uint16_t* x, const uint16_t* w_gate, int 
   if (!make_bf16_map(&tm_x, x, static_cast<uint64_t>(T), static_cast<uint64_t>(H), 128)) return MOE_ERR_CUDA;
   if (!make_bf16_map(&tm_w, w_gate, static_cast<uint64_t>(E), static_cast<uint64_t>(H), static_cast<uint32_t>(s.NE)))
     return MOE_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int nv = (s.NE + 31) / 32;
   moe_status rs = nv <= 1   ? launch_router<1>(tm_x, tm_w, p, s.tiles, s.splits, st)
                   : nv <= 2 ? launch_router<2>(tm_x, tm_w, p, s.tiles, s.splits, st)
