@@ -129,11 +129,7 @@ MOE_DEVINL void block_dst(uint8_t* codes, uint8_t* sf, int64_t dst, int c, int K
 
 // Quantises one 16-element block: codes of elements 0-7 in *lo, 8-15 in *hi
 // (element 2i in the low nibble of byte i), returns the e4m3 scale byte.
-template <int IN_F32>
-MOE_DEVINL uint32_t quantize_block16(const void* x, int64_t row, int K, int blk, float s, uint32_t* lo,
-                                     uint32_t* hi) {
-  float v[16];
-  load_block16<IN_F32>(x, row, K, blk, v);
+MOE_DEVINL uint32_t quantize_values16(const float (&v)[16], float s, uint32_t* lo, uint32_t* hi) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -142,6 +138,14 @@ MOE_DEVINL uint32_t quantize_block16(const void* x, int64_t row, int K, int blk,
   *lo = nvfp4_codes8(v, recip);
   *hi = nvfp4_codes8(v + 8, recip);
   return sfb;
+}
+
+template <int IN_F32>
+MOE_DEVINL uint32_t quantize_block16(const void* x, int64_t row, int K, int blk, float s, uint32_t* lo,
+                                     uint32_t* hi) {
+  float v[16];
+  load_block16<IN_F32>(x, row, K, blk, v);
+  return quantize_values16(v, s, lo, hi);
 }
 
 // One warp per source row.  The row is quantised once and written to every
@@ -185,8 +189,32 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
     uint32_t c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     uint32_t sf4 = 0;
     if (act) {
+      if (IN_F32) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) sf4 |= quantize_block16<IN_F32>(x, src, K, 4 * q + b, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
+        for (int b = 0; b < 4; ++b)
+          sf4 |= quantize_block16<IN_F32>(x, src, K, 4 * q + b, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
+      } else {
+        // the lane's 128 bytes of bf16 x requested together before any arithmetic: one memory round trip
+        // per warp instead of one per block
+        const uint4* p4 = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + src * K + 64 * q);
+        uint4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) raw[i] = __ldg(p4 + i);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const uint32_t w[4] = {raw[2 * b + i].x, raw[2 * b + i].y, raw[2 * b + i].z, raw[2 * b + i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+              v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+          }
+          sf4 |= quantize_values16(v, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
+        }
+      }
     }
     if (LAYOUT != 2) {
       // Linear codes: the slice's codes form one contiguous span of 32 B per quad.  Lane l
