@@ -113,8 +113,9 @@ MOE_API void moe_set_wait_timeout_ns(uint64_t ns);
 
 /* Test hooks: bit 0 makes the next grouped-GEMM launches skip filling their
  * first pipeline stage (and moe_router's first CTA skip its first), so the
- * bounded-wait path can be exercised without faulting anything; bit 1 makes them keep the one-CTA 128-row tile where
- * the CTA-pair tile would run, so both kernels can be compared on one input;
+ * bounded-wait path can be exercised without faulting anything; bit 1 makes
+ * them keep the one-CTA 128-row tile where the CTA-pair tile would run, so
+ * both kernels can be compared on one input;
  * bit 2 makes moe_forward (and its graph) use the staged kernels for layers
  * the single-launch path would take.  0 (the default) for normal operation. */
 MOE_API void moe_debug_set_flags(int flags);
@@ -194,8 +195,11 @@ MOE_API moe_status moe_route_permute_static(const float* logits, int T, int E, i
  *   linear gate.
  * The K = H sum is split into contiguous ranges whose FP32 partial sums are
  * added in range order, so the logits (and everything routed from them) are
- * the same on every call with the same inputs; they differ from a sequential
- * sum only by FP32 rounding order.
+ * the same on every call with the same inputs on the same device; they differ
+ * from a sequential sum only by FP32 rounding order.  The number of ranges
+ * (up to 16) follows from T, H and how many CTA clusters the device holds; a
+ * call made while its stream is being captured, before any other call on that
+ * device, takes at most 8.
  * Arguments (device pointers unless noted):
  *   x        bf16 [T][H] (raw bits), 16-byte aligned
  *   w_gate   bf16 [E][H], 16-byte aligned
