@@ -245,6 +245,29 @@ def test_router_matches_oracle(T, E, k, H):
         assert srt[k - 1] - srt[k] <= 2 * bound[t].max(), t
 
 
+def test_router_one_split_without_logits_output():
+    """With 80 or more 128-token tiles each tile gets one K split, and without a logits output the owner CTA
+    routes straight from its drained accumulator (no split sum pass): the routing must be the one of the call
+    that also writes the logits, which is the oracle's routing of those logits."""
+    T, E, k, H = 10240, 64, 4, 256
+    x = inputs.activations(T, H, seed=11)
+    wg = inputs.router_gate(E, H)
+    xd, wgd = x.to(DEV), wg.to(DEV)
+    xs1 = torch.zeros(1, dtype=torch.float32, device=DEV)
+    xs2 = torch.zeros(1, dtype=torch.float32, device=DEV)
+    r1, lg = moe.moe_router(xd, wgd, k, x_scale=xs1)
+    r2, none = moe.moe_router(xd, wgd, k, want_logits=False, x_scale=xs2)
+    torch.cuda.synchronize()
+    assert none is None
+    assert moe.device_error() == (0, 0)
+    ids, w = oracle.route(lg.cpu().numpy(), k)
+    assert np.array_equal(r1.topk_id.cpu().numpy(), ids)
+    assert np.array_equal(r1.topk_w.cpu().numpy().view(np.uint32), w.view(np.uint32))
+    for f in ("topk_id", "topk_w", "expert_offsets", "perm_to_expanded", "expanded_to_perm", "expanded_to_row"):
+        assert torch.equal(getattr(r1, f), getattr(r2, f)), f
+    assert xs1.item() == xs2.item() == np.float32(oracle.tensor_scale_from_amax(oracle.amax(x.float().numpy())))
+
+
 def test_router_timeout_path_reports_and_recovers():
     """The router's first CTA never fills its first stage: its bounded waits give up, the launch reports
     MOE_ERR_TIMEOUT, and that CTA's tile is void in every CTA of its cluster, so the tile's tokens go to
