@@ -209,11 +209,12 @@ def test_finalize_matches_oracle(T, k, N):
 
 # the router kernel's K splits per 128-token tile (a cluster of that many CTAs): 4 (16, 200 and 2000 tokens),
 # 8 (129 and 100 tokens), 16 where the GPU holds every tile's 16-CTA cluster at once, else 8 (300, 256 and 1024
-# tokens), 2 (6144 tokens: 48 tiles); E = 40 and E = 200 leave a partial 32-expert lane group; k = 32 makes
+# tokens; 256 tokens with E = 200 and 8 K blocks per split), 2 (6144 tokens: 48 tiles); E = 40 and E = 200 leave a
+# partial 32-expert lane group; k = 32 makes
 # 8-token chunks (two per owner CTA at 8 splits, one at 16), k = 1 one chunk per owner
 @pytest.mark.parametrize("T,E,k,H", [(16, 8, 2, 256), (129, 40, 4, 512), (300, 256, 8, 1024), (1024, 256, 8, 6144),
                                      (6144, 256, 8, 512), (100, 256, 32, 512), (256, 256, 32, 1024),
-                                     (200, 64, 1, 256), (2000, 200, 6, 256)])
+                                     (256, 200, 6, 2048), (200, 64, 1, 256), (2000, 200, 6, 256)])
 def test_router_matches_oracle(T, E, k, H):
     """Logits within the FP32 summation-order bound of the oracle's FP64 sums; the routing is exactly the
     oracle's routing of the GPU's logits, and agrees with the oracle's own logits except at near-ties."""
