@@ -22,6 +22,17 @@ namespace {
 
 constexpr int kQuantWarps = 8;
 
+// Eight bf16 values (one 16-byte word, element 2i in the low half of 32-bit
+// word i) as FP32, exactly.
+MOE_DEVINL void bf16x8_to_f32(const uint4& u, float* v) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
 template <int IN_F32>
 MOE_DEVINL void load_block16(const void* x, int64_t row, int K, int blk, float (&v)[16]) {
   if (IN_F32) {
@@ -34,15 +45,7 @@ MOE_DEVINL void load_block16(const void* x, int64_t row, int K, int blk, float (
   } else {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + row * K + blk * 16);
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      uint4 u = __ldg(p + i);
-      uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-        v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-    }
+    for (int i = 0; i < 2; ++i) bf16x8_to_f32(__ldg(p + i), v + 8 * i);
   }
 }
 
@@ -203,15 +206,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32) quantize_kernel(
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           float v[16];
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const uint32_t w[4] = {raw[2 * b + i].x, raw[2 * b + i].y, raw[2 * b + i].z, raw[2 * b + i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-              v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-            }
-          }
+          bf16x8_to_f32(raw[2 * b], v);
+          bf16x8_to_f32(raw[2 * b + 1], v + 8);
           sf4 |= quantize_values16(v, s, &c[2 * b], &c[2 * b + 1]) << (8 * b);
         }
       }
